@@ -1,0 +1,132 @@
+/*
+ * rq_oracle.h -- plain CPU oracle for the fused residual-add + RMSNorm +
+ * FP8 / NVFP4 quantisation path and the per-head Q/K RMSNorm + RoPE + FP8
+ * store.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This is a slow, single-threaded, obviously
+ * correct restatement of what the path computes.  Only the tests, the smoke
+ * check and the benchmark's CPU-baseline leg load it.  The CUDA library shares
+ * no code, header, table or helper with it, and never calls it.
+ *
+ * Sources (pages, by title and section):
+ *   [P1] "Add NanoJet backend for AutoDeploy prefill-only FP8 inference"
+ *        (TensorRT-LLM PR 17288), Description: RMSNorm with FP8 quantisation
+ *        in the epilogue; fused Q/K RMSNorm and RoPE.
+ *   [P2] "Add AutoDeploy NVFP4 RMSNorm quant fusion" (TensorRT-LLM PR 14361),
+ *        Walkthrough / Changes: fused add + RMSNorm + NVFP4 ops, with and
+ *        without the high-precision norm output.
+ *   [P3] "perf: add fused norm + RoPE + uniform fp8 store for TRT-LLM DSv4
+ *        sparse attention" (SGLang PR 32975), review thread: norm + RoPE +
+ *        uniform FP8 store.
+ *   [P4] "[Performance]: Fuse local NVFP4 tail after NCCL fallback"
+ *        (TensorRT-LLM issue 17900), Proposal: residual + RMSNorm (+ norm
+ *        output) + NVFP4 in one pass; support conditions (FP16/BF16, FP32
+ *        per-tensor scale, hidden % 16 == 0).
+ * The pages give the operations but not their rounding points; the readings
+ * taken here (quantise from the dtype-rounded norm output, eps inside the
+ * square root, plain multiply by the weight, IEEE division by the FP8 scale,
+ * NVFP4 block scale = E4M3(gs*amax/6), encode factor gs/scale) are the plain
+ * ones and are listed in the design notes.
+ *
+ * Storage types: bfloat16 / float16 are passed as uint16_t bit patterns,
+ * E4M3 and packed E2M1 as uint8_t.  Every fp32 step is a C `float`
+ * operation compiled with -ffp-contract=off, i.e. one IEEE single rounding
+ * (round to nearest even) per operation.
+ */
+#ifndef RQ_ORACLE_H
+#define RQ_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { RQO_BF16 = 0, RQO_FP16 = 1 };
+
+/* ---- number formats (exact decoders, round-to-nearest-even encoders) ---- */
+double   oracle_bf16_to_double(uint16_t b);
+double   oracle_fp16_to_double(uint16_t h);
+uint16_t oracle_bf16_from_double(double v);   /* RNE, overflow to +-inf */
+uint16_t oracle_fp16_from_double(double v);   /* RNE, overflow to +-inf */
+double   oracle_e4m3_to_double(uint8_t c);    /* OCP E4M3 (fn): bias 7, max 448 */
+uint8_t  oracle_e4m3_from_double(double v);   /* RNE, satfinite to +-448 */
+double   oracle_e2m1_to_double(uint8_t nib);  /* low 4 bits: sign<<3 | index */
+uint8_t  oracle_e2m1_from_double(double v);   /* RNE, satfinite to +-6 */
+
+/* Array forms of the encoders/decoders (used by the format tests). */
+void oracle_dt_from_double_array(int dt, const double *v, int64_t n, uint16_t *out);
+void oracle_dt_to_double_array(int dt, const uint16_t *b, int64_t n, double *out);
+void oracle_e4m3_from_double_array(const double *v, int64_t n, uint8_t *out);
+void oracle_e2m1_from_double_array(const double *v, int64_t n, uint8_t *out);
+
+/* ---- residual add + RMSNorm ---------------------------------------------
+ * Per row of `hidden` elements:
+ *   s_i  = dt(f32(x_i) + f32(r_i))                       -> s_out (residual')
+ *   ss   = f32(sum_i s_i^2)   (sum taken in double, rounded once)
+ *   rstd = f32(1 / f32(sqrt(f32(f32(ss / hidden) + eps))))
+ *   y_i  = dt(f32(f32(s_i * rstd) * w_i))                -> y_out (norm out)
+ * s_out may equal r (in place).  y_out may be NULL. */
+void oracle_add_rmsnorm(int dt, const uint16_t *x, const uint16_t *r,
+                        const uint16_t *w, float eps, int64_t rows,
+                        int64_t hidden, uint16_t *s_out, uint16_t *y_out);
+
+/* Per-tensor FP8: q_i = E4M3sat(f32(y_i / scale)); scale is the dequant
+ * scale (x ~= e4m3(q) * scale). */
+void oracle_quant_fp8(int dt, const uint16_t *y, int64_t n, float scale,
+                      uint8_t *q);
+
+/* NVFP4 over rows of `hidden` (hidden % 16 == 0); gs = global scale in the
+ * quantising direction (e.g. 448*6/amax).  Per 16-element block:
+ *   a   = max_i |y_i|
+ *   sf  = E4M3sat(f32(f32(gs * a) / 6))                  -> sf[row*hidden/16+b]
+ *   enc = (sf == 0) ? 0 : f32(gs / sf)
+ *   c_i = E2M1sat(f32(y_i * enc)),  byte j = c_2j | c_2j+1 << 4 -> packed
+ * Dequantised value: e2m1(c_i) * sf / gs. */
+void oracle_quant_nvfp4(int dt, const uint16_t *y, int64_t rows,
+                        int64_t hidden, float gs, uint8_t *packed,
+                        uint8_t *sf);
+
+/* Whole fused calls: residual add + RMSNorm, then the quantiser. */
+void oracle_add_rmsnorm_fp8(int dt, const uint16_t *x, const uint16_t *r,
+                            const uint16_t *w, float eps, float scale,
+                            int64_t rows, int64_t hidden, uint16_t *s_out,
+                            uint16_t *y_out, uint8_t *q);
+void oracle_add_rmsnorm_nvfp4(int dt, const uint16_t *x, const uint16_t *r,
+                              const uint16_t *w, float eps, float gs,
+                              int64_t rows, int64_t hidden, uint16_t *s_out,
+                              uint16_t *y_out, uint8_t *packed, uint8_t *sf);
+
+/* max_i |v_i| of a dtype tensor (exact), and the calibrated scales. */
+float oracle_amax(int dt, const uint16_t *v, int64_t n);
+float oracle_fp8_scale_from_amax(float amax);    /* f32(amax / 448)  */
+float oracle_nvfp4_gs_from_amax(float amax);     /* f32(2688 / amax) */
+
+/* ---- per-head Q/K RMSNorm + NeoX RoPE (+ FP8) -----------------------------
+ * src: n_tokens tokens, token t starts at src + t*token_stride elements and
+ * holds n_heads contiguous heads of head_dim elements.  For each head:
+ *   n   = RMSNorm of the head (same steps as above, weight w[head_dim],
+ *         no residual), rounded to dt
+ *   p   = clamp(pos[t], 0, max_pos-1); c_i = cs[p][i], s_i = cs[p][half+i]
+ *   o_i        = dt(f32(f32(n_i * c_i) - f32(n_{i+half} * s_i)))
+ *   o_{i+half} = dt(f32(f32(n_{i+half} * c_i) + f32(n_i * s_i)))
+ * with half = head_dim/2 and cs a [max_pos, head_dim] fp32 table
+ * (cos in the first half, sin in the second).  o is written densely as
+ * [n_tokens, n_heads, head_dim]. */
+void oracle_qk_rmsnorm_rope(int dt, const uint16_t *src, int64_t token_stride,
+                            int64_t n_tokens, int n_heads, int head_dim,
+                            const uint16_t *w, float eps, const int32_t *pos,
+                            const float *cos_sin, int64_t max_pos,
+                            uint16_t *o);
+/* The above followed by oracle_quant_fp8 with `scale`. */
+void oracle_qk_rmsnorm_rope_fp8(int dt, const uint16_t *src,
+                                int64_t token_stride, int64_t n_tokens,
+                                int n_heads, int head_dim, const uint16_t *w,
+                                float eps, const int32_t *pos,
+                                const float *cos_sin, int64_t max_pos,
+                                float scale, uint16_t *o, uint8_t *q);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RQ_ORACLE_H */
