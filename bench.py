@@ -1,0 +1,485 @@
+"""Benchmark of the fused norm + quant prologue on GB300.
+
+One step runs the whole hot path once over one batch of seeded synthetic
+inputs, one call per fused kernel:
+  * residual add + RMSNorm + FP8 E4M3, 65,536 rows x 1024 bf16 (64 sequences
+    of 1024 prefill tokens), static scale amax/448;
+  * per-head Q/K RMSNorm + NeoX RoPE + FP8 store, 4096 tokens x (16 Q + 8 K)
+    heads x 128 bf16, theta 1e6, per-tensor scales amax/448;
+  * residual add + RMSNorm + NVFP4 with bf16 norm output, 16,384 rows x 7168
+    bf16 (x with 1 % outliers x20), global scale 2688/amax.
+The scales are calibrated once before timing with the library's own amax
+kernels.  `value` is rows per second over the step (a Q/K "row" is one head
+of one token); per-kernel rows/s and HBM GB/s come from CUDA events around
+each launch.  Every step's inputs were last touched more than 1 GB of traffic
+earlier, so they are not L2 resident (L2 is 129 MB).
+
+  python bench.py [--steps K] [--warmup W] [--gpus N] [--impl reference]
+
+--impl reference times the CPU oracle on a bounded sample of the same
+workload (the reference arm).  Under torchrun every rank runs its own full
+workload (weak scaling, no collective on the data path); the timing is the
+maximum over ranks.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "rows/s and achieved HBM GB/s (% of GB300 peak) per fused norm+quant kernel, 1 GPU"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+EPS = 1e-6
+
+# (name, rows, hidden) of the two row workloads; Q/K below
+FP8_ROWS, FP8_H = 65536, 1024
+NV_ROWS, NV_H = 16384, 7168
+QK_T, QK_HQ, QK_HK, QK_D = 4096, 16, 8, 128
+
+
+def alg_bytes_fp8(rows, h):
+    # x, residual read; residual', codes written; weight and scale once
+    return rows * h * (2 + 2 + 2 + 1) + h * 2 + 4
+
+
+def alg_bytes_nvfp4(rows, h):
+    # x, residual read; residual', norm out, packed codes, block scales written
+    return rows * h * (2 + 2 + 2 + 2) + rows * h // 2 + rows * h // 16 + h * 2 + 4
+
+
+def alg_bytes_qk(t, hq, hk, d):
+    # q, k read; codes written; one cos/sin row and position per token; weights, scales
+    return t * (hq + hk) * d * (2 + 1) + t * d * 4 + t * 4 + 2 * d * 2 + 8
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(v, ws):
+    if ws == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons while timing."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dev16(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+
+
+class Workload:
+    """Device buffers of one step, and the host copies the end-to-end leg uses."""
+
+    def __init__(self, seed, pinned_host=False):
+        import nvfp4_quant_gb300 as rq
+        self.rq = rq
+        t0 = time.time()
+        x3, r3, w3 = synth.rows_input(seed, FP8_ROWS, FP8_H, "bf16", res_std=2.0)
+        x5, r5, w5 = synth.rows_input(seed, NV_ROWS, NV_H, "bf16", outlier_frac=0.01)
+        q4, k4, qw4, kw4, pos4, cs4 = synth.qk_input(seed, QK_T, QK_HQ, QK_HK, QK_D, "bf16")
+        self.gen_s = time.time() - t0
+        host = dict(x3=dev16(x3), r3=dev16(r3), x5=dev16(x5), r5=dev16(r5), q4=dev16(q4),
+                    k4=dev16(k4), pos4=torch.from_numpy(pos4))
+        self.host_in = {k: v.pin_memory() for k, v in host.items()} if pinned_host else None
+        d = {k: v.cuda() for k, v in host.items()}
+        self.d = d
+        self.w3, self.w5 = dev16(w3).cuda(), dev16(w5).cuda()
+        self.qw4, self.kw4 = dev16(qw4).cuda(), dev16(kw4).cuda()
+        self.cs4 = torch.from_numpy(cs4).cuda()
+        u8 = dict(dtype=torch.uint8, device="cuda")
+        self.ro3 = torch.empty_like(d["r3"])
+        self.q3 = torch.empty((FP8_ROWS, FP8_H), **u8)
+        self.ro5 = torch.empty_like(d["r5"])
+        self.y5 = torch.empty_like(d["x5"])
+        self.p5 = torch.empty((NV_ROWS, NV_H // 2), **u8)
+        self.sf5 = torch.empty((NV_ROWS, NV_H // 16), **u8)
+        self.qo4 = torch.empty((QK_T, QK_HQ, QK_D), **u8)
+        self.ko4 = torch.empty((QK_T, QK_HK, QK_D), **u8)
+        self.calibrate()
+
+    def calibrate(self):
+        """Static scales from the norm output's absolute maximum (library kernels)."""
+        rq, d = self.rq, self.d
+        f = lambda: torch.zeros(1, dtype=torch.float32, device="cuda")
+        a3, a5 = f(), f()
+        self.s3, self.gs5 = f(), f()
+        rq.rq_add_rmsnorm_amax(d["x3"], d["r3"], self.w3, EPS, a3)
+        rq.rq_fp8_scale_from_amax(a3, self.s3)
+        rq.rq_add_rmsnorm_amax(d["x5"], d["r5"], self.w5, EPS, a5)
+        rq.rq_nvfp4_global_scale_from_amax(a5, self.gs5)
+        # Q/K: one uniform per-tensor scale each for Q and K, amax/448 of the
+        # per-head norm output (the caller's calibration choice; the rotation
+        # keeps each pair's norm, so a few rotated values may saturate at 448)
+        self.qs4, self.ks4 = f(), f()
+        aq, ak = f(), f()
+        rq.rq_add_rmsnorm_amax(d["q4"].view(-1, QK_D), torch.zeros_like(d["q4"]).view(-1, QK_D),
+                               self.qw4, EPS, aq)
+        rq.rq_add_rmsnorm_amax(d["k4"].view(-1, QK_D), torch.zeros_like(d["k4"]).view(-1, QK_D),
+                               self.kw4, EPS, ak)
+        rq.rq_fp8_scale_from_amax(aq, self.qs4)
+        rq.rq_fp8_scale_from_amax(ak, self.ks4)
+        torch.cuda.synchronize()
+
+    # the three calls of one step
+    def fp8(self):
+        d = self.d
+        self.rq.rq_add_rmsnorm_fp8(d["x3"], d["r3"], self.ro3, self.w3, EPS, self.s3, self.q3)
+
+    def qk(self):
+        d = self.d
+        self.rq.rq_qk_rmsnorm_rope_fp8(d["q4"], d["k4"], self.qw4, self.kw4, EPS, d["pos4"],
+                                       self.cs4, self.qs4, self.ks4, self.qo4, self.ko4)
+
+    def nvfp4(self):
+        d = self.d
+        self.rq.rq_add_rmsnorm_nvfp4(d["x5"], d["r5"], self.ro5, self.w5, EPS, self.gs5, self.p5,
+                                     self.sf5, self.y5)
+
+    def outputs(self):
+        return [self.ro3, self.q3, self.qo4, self.ko4, self.ro5, self.y5, self.p5, self.sf5]
+
+
+ROWS_PER_STEP = FP8_ROWS + QK_T * (QK_HQ + QK_HK) + NV_ROWS
+KERNELS = [
+    ("add_rmsnorm_fp8", "65536x1024 bf16 -> E4M3", FP8_ROWS, alg_bytes_fp8(FP8_ROWS, FP8_H)),
+    ("qk_rmsnorm_rope_fp8", "4096 tok x (16+8) heads x 128 bf16 -> E4M3",
+     QK_T * (QK_HQ + QK_HK), alg_bytes_qk(QK_T, QK_HQ, QK_HK, QK_D)),
+    ("add_rmsnorm_nvfp4", "16384x7168 bf16 -> NVFP4 + bf16 norm out", NV_ROWS,
+     alg_bytes_nvfp4(NV_ROWS, NV_H)),
+]
+STEP_BYTES = sum(k[3] for k in KERNELS)
+
+
+def run_ours(args):
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    import nvfp4_quant_gb300 as rq
+    rq.lib()  # fail loudly if the CUDA library is missing
+
+    wl = Workload(seed=rank)
+    stream = torch.cuda.current_stream()
+    calls = [wl.fp8, wl.qk, wl.nvfp4]
+
+    for _ in range(args.warmup):
+        for c in calls:
+            c()
+    torch.cuda.synchronize()
+
+    # ---- device-resident timing: events around each launch and around all K steps
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in calls] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        time.sleep(0.3)
+        t_start.record(stream)
+        for s in range(args.steps):
+            for c, (a, b) in zip(calls, ev[s]):
+                a.record(stream)
+                c()
+                b.record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier(ws)
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), ws)
+    per_kernel_ms = [statistics.mean(ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(args.steps))
+                     for i in range(len(calls))]
+    ms_per_step = total_ms / args.steps
+    value = ROWS_PER_STEP * ws * args.steps / (total_ms / 1e3)
+
+    # ---- end to end through the public API with host buffers
+    e2e = run_e2e(args, wl, ws)
+
+    peak, peak_kind = peaks()
+    kernels = {}
+    for (name, desc, rows, nbytes), ms in zip(KERNELS, per_kernel_ms):
+        gbs = nbytes / (ms / 1e3) / 1e9
+        kernels[name] = {"workload": desc, "ms": round(ms, 5), "rows_per_s": rows / (ms / 1e3),
+                         "alg_bytes": nbytes, "gbs": round(gbs, 1),
+                         "frac_of_measured_peak": round(gbs / peak, 4),
+                         "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4)}
+    dom = max(range(len(KERNELS)), key=lambda i: per_kernel_ms[i])
+    dname, _, _, dbytes = KERNELS[dom]
+    dgbs = kernels[dname]["gbs"]
+    traffic = load_traffic(dname)
+
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "rows/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded splitmix64 normals, rounded to bf16)",
+        "config": {
+            "workload": "fused norm+quant prologue step: add_rmsnorm_fp8 65536x1024 bf16 + "
+                        "qk_rmsnorm_rope_fp8 4096 tok x (16+8) heads x 128 bf16 + "
+                        "add_rmsnorm_nvfp4 16384x7168 bf16 with bf16 norm out",
+            "rows_per_step": ROWS_PER_STEP,
+            "row_note": "a Q/K row is one 128-element head of one token",
+            "alg_bytes_per_step": STEP_BYTES,
+            "step_gbs": round(STEP_BYTES / (ms_per_step / 1e3) / 1e9, 1),
+            "l2": "no flush: each kernel's inputs were last touched > 1 GB of HBM traffic "
+                  "earlier (L2 129 MB), residual written out of place so every step is identical",
+            "parallelism": "replicas" if ws > 1 else "single GPU",
+        },
+        "kernels": kernels,
+        "roofline": {"kernel": dname, "bound": "hbm", "achieved": dgbs, "peak": peak,
+                     "unit": "GB/s", "frac": round(dgbs / peak, 4), "peak_kind": peak_kind,
+                     "frac_of_nominal_8tbs": round(dgbs / NOMINAL_HBM_GBS, 4),
+                     "traffic": traffic, "alg_bytes": dbytes},
+        "e2e": e2e,
+        "gpu_launches": len(calls) * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(args, wl, ws):
+    """Same step through the public API with pinned host inputs and outputs:
+    every step copies its activations host -> device and reads every output
+    back, inside the timed region."""
+    host_in = {k: v.pin_memory() for k, v in
+               {k: wl.d[k].cpu() for k in ("x3", "r3", "x5", "r5", "q4", "k4", "pos4")}.items()}
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in wl.outputs()]
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for k, v in host_in.items():
+            wl.d[k].copy_(v, non_blocking=True)
+        wl.fp8()
+        wl.qk()
+        wl.nvfp4()
+        for h, d in zip(host_out, wl.outputs()):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    n = max(1, min(args.steps, 10))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    a.record(stream)
+    for _ in range(n):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b), ws) / n
+    return {"value": ROWS_PER_STEP * ws / (ms / 1e3), "unit": "rows/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def load_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary of this kernel, if
+    it exists and matches the current source hash; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        ent = d.get(kernel)
+        if ent and ent.get("source_hash") == source_hash():
+            return ent["dram_bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
+def source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "nvfp4_quant_gb300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, n), "rb") as f:
+            h.update(n.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_step_sample(frac_rows):
+    """Time the oracle on a sample of each call of the step; returns
+    (seconds per full step extrapolated by rows, sample description)."""
+    import oracle as O
+    r3 = max(1, int(FP8_ROWS * frac_rows))
+    r5 = max(1, int(NV_ROWS * frac_rows))
+    t4 = max(1, int(QK_T * frac_rows))
+    x3, rr3, w3 = synth.rows_input(0, r3, FP8_H, "bf16", res_std=2.0)
+    x5, rr5, w5 = synth.rows_input(0, r5, NV_H, "bf16", outlier_frac=0.01)
+    q4, k4, qw4, kw4, pos4, cs4 = synth.qk_input(0, t4, QK_HQ, QK_HK, QK_D, "bf16")
+    O.lib()
+    t = time.perf_counter()
+    O.add_rmsnorm_fp8("bf16", x3, rr3, w3, EPS, 0.01)
+    t_fp8 = time.perf_counter() - t
+    t = time.perf_counter()
+    O.qk_rmsnorm_rope_fp8("bf16", q4.reshape(-1), QK_HQ * QK_D, t4, QK_HQ, QK_D, qw4, EPS, pos4, cs4, 0.01)
+    O.qk_rmsnorm_rope_fp8("bf16", k4.reshape(-1), QK_HK * QK_D, t4, QK_HK, QK_D, kw4, EPS, pos4, cs4, 0.01)
+    t_qk = time.perf_counter() - t
+    t = time.perf_counter()
+    O.add_rmsnorm_nvfp4("bf16", x5, rr5, w5, EPS, 400.0)
+    t_nv = time.perf_counter() - t
+    full = t_fp8 * FP8_ROWS / r3 + t_qk * QK_T / t4 + t_nv * NV_ROWS / r5
+    desc = ("oracle (single-threaded C) on %d of %d FP8 rows, %d of %d Q/K tokens, %d of %d "
+            "NVFP4 rows; time scaled to a full step by rows" % (r3, FP8_ROWS, t4, QK_T, r5, NV_ROWS))
+    return full, t_fp8 + t_qk + t_nv, desc
+
+
+def cpu_baseline(target_seconds):
+    # size the sample so the oracle runs about target_seconds
+    full, spent, _ = oracle_step_sample(1.0 / 256)
+    frac = min(1.0, (1.0 / 256) * target_seconds / max(spent, 1e-3))
+    full, spent, desc = oracle_step_sample(frac)
+    return {"value": ROWS_PER_STEP / full, "unit": "rows/s", "cores": 1, "kind": "oracle",
+            "sample": desc + " (%.1f s of CPU work)" % spent}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    frac = args.ref_fraction
+    for _ in range(args.warmup):
+        oracle_step_sample(frac)
+    fulls, spents = [], []
+    for _ in range(args.steps):
+        full, spent, desc = oracle_step_sample(frac)
+        fulls.append(full)
+        spents.append(spent)
+    ms = statistics.mean(fulls) * 1e3
+    value = ROWS_PER_STEP / (ms / 1e3)
+    line = {
+        "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded splitmix64 normals)",
+        "impl": "reference",
+        "config": {"workload": "fused norm+quant prologue step: add_rmsnorm_fp8 65536x1024 bf16 + "
+                               "qk_rmsnorm_rope_fp8 4096 tok x (16+8) heads x 128 bf16 + "
+                               "add_rmsnorm_nvfp4 16384x7168 bf16 with bf16 norm out",
+                   "rows_per_step": ROWS_PER_STEP},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                         "sample": desc + " per step"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-fraction", type=float, default=1.0 / 128)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        print("bench: at least 3 warm-up steps are required", file=sys.stderr)
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,187 @@
+/*
+ * rq.h -- C ABI of librq: fused residual add + RMSNorm + FP8 / NVFP4
+ * quantisation, and per-head Q/K RMSNorm + RoPE + FP8 store, for NVIDIA
+ * GB300 (sm_103a).
+ *
+ * Conventions for every entry point
+ *  - All tensor pointers are DEVICE pointers owned by the caller, row-major
+ *    and contiguous unless a stride argument says otherwise.  The library
+ *    allocates no device memory and keeps no state besides a per-device cache
+ *    of launch limits.
+ *  - Scales are fp32 scalars in device memory, read by the kernel, so a call
+ *    never synchronises with the host.
+ *  - Work is enqueued on `stream` (NULL = the legacy default stream) and is
+ *    asynchronous: a returned RQ_OK means the launch was accepted.
+ *  - Every argument check runs on the host before any CUDA call; a failed
+ *    check returns an error status and launches nothing.  Nothing throws
+ *    across the ABI.  rows == 0 (or n_tokens == 0) returns RQ_OK and launches
+ *    nothing.
+ *  - Alignment: every tensor pointer must be 16-byte aligned; scalar pointers
+ *    4-byte aligned.
+ *  - Aliasing: residual_out may equal residual_in exactly (in-place residual
+ *    update); any other overlap between an output and another argument
+ *    returns RQ_ERR_ALIAS.
+ *
+ * Numerics (every fp32 step is one IEEE round-to-nearest-even operation; the
+ * only freedom is the order of the fp32 sum of squares):
+ *   s_i  = dt(x_i + r_i)                                   (residual')
+ *   rstd = 1 / sqrt(sum_i s_i^2 / hidden + eps)
+ *   y_i  = dt((s_i * rstd) * w_i)                          (norm output)
+ *   FP8:   q_i = E4M3(y_i / scale)           round to nearest even, satfinite
+ *   NVFP4: per 16-element block, a = max |y_i|,
+ *          sf = E4M3((gs * a) / 6), enc = gs / sf (0 if sf == 0),
+ *          c_i = E2M1(y_i * enc), packed two per byte, even element in the
+ *          low nibble; dequantised value = e2m1(c_i) * sf / gs.
+ */
+#ifndef RQ_H
+#define RQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared here so that the header needs no
+ * CUDA include. */
+struct CUstream_st;
+typedef struct CUstream_st *rq_stream_t;
+
+typedef enum {
+    RQ_OK = 0,
+    RQ_ERR_NULL = 1,        /* a required pointer is NULL */
+    RQ_ERR_SHAPE = 2,       /* rows < 0, hidden <= 0 or % 16 != 0, bad stride ... */
+    RQ_ERR_DTYPE = 3,       /* dtype is neither RQ_BF16 nor RQ_FP16 */
+    RQ_ERR_MISALIGNED = 4,  /* a pointer or stride breaks the 16-byte rule */
+    RQ_ERR_ALIAS = 5,       /* an output overlaps another argument */
+    RQ_ERR_UNSUPPORTED = 6, /* hidden > RQ_MAX_HIDDEN, head_dim != 128 ... */
+    RQ_ERR_CUDA = 7         /* the CUDA runtime refused the launch; see rq_last_error() */
+} rq_status;
+
+/* Storage type of x, residual, weight and norm_out (all must match). */
+typedef enum { RQ_BF16 = 0, RQ_FP16 = 1 } rq_dtype;
+
+#define RQ_MAX_HIDDEN 32768
+#define RQ_QK_HEAD_DIM 128
+
+/*
+ * Residual add + RMSNorm + per-tensor FP8 E4M3.
+ * Source: "Add NanoJet backend for AutoDeploy prefill-only FP8 inference"
+ * (TensorRT-LLM PR 17288), Description: RMSNorm with FP8 quantisation in the
+ * kernel epilogue; residual add folded in place (same page, Test Coverage:
+ * residual folding with aliasing).
+ *
+ *   x, residual_in      [rows, hidden] dt, read
+ *   residual_out        [rows, hidden] dt, written with s (may == residual_in)
+ *   weight              [hidden] dt
+ *   d_scale             device fp32 dequant scale (q = y / scale)
+ *   q_out               [rows, hidden] E4M3 bytes
+ *   norm_out            [rows, hidden] dt, written with y; may be NULL
+ *   hidden              multiple of 16, <= RQ_MAX_HIDDEN
+ */
+rq_status rq_add_rmsnorm_fp8(const void *x, const void *residual_in,
+                             void *residual_out, const void *weight,
+                             float eps, const float *d_scale, uint8_t *q_out,
+                             void *norm_out, int64_t rows, int64_t hidden,
+                             rq_dtype dt, rq_stream_t stream);
+
+/*
+ * Residual add + RMSNorm (+ high-precision norm output) + NVFP4.
+ * Source: "Add AutoDeploy NVFP4 RMSNorm quant fusion" (TensorRT-LLM PR 14361),
+ * Changes: fused add + RMSNorm + NVFP4 ops with and without the norm output;
+ * "[Performance]: Fuse local NVFP4 tail after NCCL fallback" (TensorRT-LLM
+ * issue 17900), Proposal: the one-launch residual + RMSNorm + NVFP4 tail and
+ * its support conditions (FP16/BF16 contiguous matching dtypes, FP32 scalar
+ * per-tensor scale, no bias, hidden % 16 == 0).
+ *
+ *   d_global_scale      device fp32 gs in the quantising direction (e.g.
+ *                       448 * 6 / amax(y))
+ *   q_packed            [rows, hidden / 2] bytes (rq_nvfp4_packed_bytes)
+ *   block_scales        [rows, hidden / 16] E4M3 bytes, row-major
+ *                       (rq_nvfp4_scale_bytes)
+ *   other arguments as in rq_add_rmsnorm_fp8
+ */
+rq_status rq_add_rmsnorm_nvfp4(const void *x, const void *residual_in,
+                               void *residual_out, const void *weight,
+                               float eps, const float *d_global_scale,
+                               uint8_t *q_packed, uint8_t *block_scales,
+                               void *norm_out, int64_t rows, int64_t hidden,
+                               rq_dtype dt, rq_stream_t stream);
+
+/*
+ * Per-head Q/K RMSNorm + NeoX RoPE + uniform FP8 E4M3 store.
+ * Source: "Add NanoJet backend for AutoDeploy prefill-only FP8 inference",
+ * Description (fused Q/K RMSNorm and RoPE); "perf: add fused norm + RoPE +
+ * uniform fp8 store for TRT-LLM DSv4 sparse attention" (SGLang PR 32975),
+ * review thread (norm, RoPE and a uniform FP8 store in one kernel).
+ *
+ *   q, k                token t, head h starts at q + t*q_token_stride +
+ *                       h*head_dim elements (strides in elements, multiples
+ *                       of 8, >= n_heads*head_dim); heads are contiguous
+ *   q_weight, k_weight  [head_dim] dt, shared by all heads of Q (resp. K)
+ *   positions           [n_tokens] int32; values outside [0, max_pos) are
+ *                       clamped into it
+ *   cos_sin_cache       [max_pos, head_dim] fp32: cos of the head_dim/2
+ *                       frequencies, then their sin
+ *   d_q_scale, d_k_scale device fp32 dequant scales (may be the same pointer)
+ *   q_out, k_out        [n_tokens, n_*_heads, head_dim] E4M3 bytes (dense)
+ *   head_dim            must be RQ_QK_HEAD_DIM (128)
+ *   n_q_heads or n_k_heads may be 0, in which case that side's pointers may
+ *   be NULL.
+ * Per head: n = dt(RMSNorm(x) * w); o_i = dt(n_i c_i - n_{i+64} s_i),
+ * o_{i+64} = dt(n_{i+64} c_i + n_i s_i); out = E4M3(o / scale).
+ */
+rq_status rq_qk_rmsnorm_rope_fp8(const void *q, const void *k,
+                                 int64_t q_token_stride,
+                                 int64_t k_token_stride, int64_t n_tokens,
+                                 int n_q_heads, int n_k_heads, int head_dim,
+                                 const void *q_weight, const void *k_weight,
+                                 float eps, const int32_t *positions,
+                                 const float *cos_sin_cache, int64_t max_pos,
+                                 const float *d_q_scale,
+                                 const float *d_k_scale, uint8_t *q_out,
+                                 uint8_t *k_out, rq_dtype dt,
+                                 rq_stream_t stream);
+
+/*
+ * Calibration: d_amax = max over the tensor of |y| (the norm output the
+ * fused calls would produce), written to one device fp32.  Nothing else is
+ * written.  The call clears d_amax on `stream` first.
+ * Source: the per-tensor scales the pages use are derived from the norm
+ * output's absolute maximum ("Add AutoDeploy NVFP4 RMSNorm quant fusion",
+ * Changes: reference module with input-scale calibration).
+ */
+rq_status rq_add_rmsnorm_amax(const void *x, const void *residual_in,
+                              const void *weight, float eps, float *d_amax,
+                              int64_t rows, int64_t hidden, rq_dtype dt,
+                              rq_stream_t stream);
+
+/* d_scale = amax / 448 (the FP8 dequant scale) and d_gs = 448 * 6 / amax
+ * (the NVFP4 global scale), each one fp32 division on the device. */
+rq_status rq_fp8_scale_from_amax(const float *d_amax, float *d_scale,
+                                 rq_stream_t stream);
+rq_status rq_nvfp4_global_scale_from_amax(const float *d_amax, float *d_gs,
+                                          rq_stream_t stream);
+
+/* Output sizes of the NVFP4 call (the linear, unswizzled layout):
+ * rows * hidden / 2 packed bytes and rows * hidden / 16 scale bytes.
+ * Source: "Add AutoDeploy NVFP4 RMSNorm quant fusion", review: the packed
+ * output and scale-tensor size math of the fake (shape-only) ops. */
+size_t rq_nvfp4_packed_bytes(int64_t rows, int64_t hidden);
+size_t rq_nvfp4_scale_bytes(int64_t rows, int64_t hidden);
+
+/* Text of a status code (static storage). */
+const char *rq_status_string(rq_status status);
+
+/* Message of the last RQ_ERR_CUDA returned on the calling thread (static,
+ * thread-local storage; "" if none). */
+const char *rq_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int rq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RQ_H */

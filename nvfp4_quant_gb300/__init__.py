@@ -1,0 +1,201 @@
+"""nvfp4_quant_gb300: Python binding of librq, the GB300 (sm_103a) library of
+fused residual add + RMSNorm + FP8 / NVFP4 quantisation kernels and the
+per-head Q/K RMSNorm + RoPE + FP8 store.
+
+This module only marshals arguments: it turns torch CUDA tensors into device
+pointers and sizes, calls the C ABI (include/rq.h) through ctypes, and raises
+RQError when a call returns a non-OK status.  Every step of the computation
+runs in the CUDA kernels of librq.so; there is no other code path.  If the
+library has not been built, importing works but the first call raises.
+"""
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "lib", "librq.so")
+
+RQ_BF16, RQ_FP16 = 0, 1
+RQ_MAX_HIDDEN = 32768
+RQ_QK_HEAD_DIM = 128
+STATUS = {0: "RQ_OK", 1: "RQ_ERR_NULL", 2: "RQ_ERR_SHAPE", 3: "RQ_ERR_DTYPE",
+          4: "RQ_ERR_MISALIGNED", 5: "RQ_ERR_ALIAS", 6: "RQ_ERR_UNSUPPORTED", 7: "RQ_ERR_CUDA"}
+
+# exported symbol -> (restype, argtypes)
+_vp, _i64, _f32, _int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int
+SIGNATURES = {
+    "rq_add_rmsnorm_fp8": (_int, [_vp, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _i64, _i64, _int, _vp]),
+    "rq_add_rmsnorm_nvfp4": (_int, [_vp, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _i64, _i64,
+                                    _int, _vp]),
+    "rq_qk_rmsnorm_rope_fp8": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp, _vp,
+                                      _f32, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _int, _vp]),
+    "rq_add_rmsnorm_amax": (_int, [_vp, _vp, _vp, _f32, _vp, _i64, _i64, _int, _vp]),
+    "rq_fp8_scale_from_amax": (_int, [_vp, _vp, _vp]),
+    "rq_nvfp4_global_scale_from_amax": (_int, [_vp, _vp, _vp]),
+    "rq_nvfp4_packed_bytes": (ctypes.c_size_t, [_i64, _i64]),
+    "rq_nvfp4_scale_bytes": (ctypes.c_size_t, [_i64, _i64]),
+    "rq_status_string": (ctypes.c_char_p, [_int]),
+    "rq_last_error": (ctypes.c_char_p, []),
+    "rq_version": (_int, []),
+}
+
+_lib = None
+
+
+class RQError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__(message)
+        self.status = status
+
+
+def lib():
+    """The loaded librq.so (ctypes); raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("librq.so is not built (%s); run "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(status):
+    if status != 0:
+        L = lib()
+        msg = L.rq_status_string(status).decode()
+        if status == 7:
+            msg += " (" + L.rq_last_error().decode() + ")"
+        raise RQError(status, msg)
+
+
+def _dt(t):
+    if t.dtype == torch.bfloat16:
+        return RQ_BF16
+    if t.dtype == torch.float16:
+        return RQ_FP16
+    raise ValueError("tensors must be bfloat16 or float16, got %s" % t.dtype)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def _rows(x, *others):
+    if x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous [rows, hidden] tensor")
+    for o in others:
+        if o is not None and (o.shape != x.shape or o.dtype != x.dtype or not o.is_contiguous()):
+            raise ValueError("residual / norm_out must match x in shape, dtype and be contiguous")
+    return x.shape[0], x.shape[1]
+
+
+def rq_add_rmsnorm_fp8(x, residual_in, residual_out, weight, eps, scale, q_out,
+                       norm_out=None, stream=None):
+    """Residual add + RMSNorm + per-tensor FP8 E4M3 (include/rq.h).
+    scale: 1-element float32 CUDA tensor (dequant scale); q_out: uint8 [rows, hidden]."""
+    rows, hidden = _rows(x, residual_in, residual_out, norm_out)
+    if weight.dtype != x.dtype:
+        raise ValueError("weight dtype must match x")
+    _check(lib().rq_add_rmsnorm_fp8(_ptr(x), _ptr(residual_in), _ptr(residual_out), _ptr(weight),
+                                    float(eps), _ptr(scale), _ptr(q_out), _ptr(norm_out),
+                                    rows, hidden, _dt(x), _stream(stream)))
+
+
+def rq_add_rmsnorm_nvfp4(x, residual_in, residual_out, weight, eps, global_scale, q_packed,
+                         block_scales, norm_out=None, stream=None):
+    """Residual add + RMSNorm (+ norm out) + NVFP4 (include/rq.h).
+    q_packed: uint8 [rows, hidden/2]; block_scales: uint8 [rows, hidden/16]."""
+    rows, hidden = _rows(x, residual_in, residual_out, norm_out)
+    if weight.dtype != x.dtype:
+        raise ValueError("weight dtype must match x")
+    _check(lib().rq_add_rmsnorm_nvfp4(_ptr(x), _ptr(residual_in), _ptr(residual_out),
+                                      _ptr(weight), float(eps), _ptr(global_scale),
+                                      _ptr(q_packed), _ptr(block_scales), _ptr(norm_out),
+                                      rows, hidden, _dt(x), _stream(stream)))
+
+
+def rq_add_rmsnorm_amax(x, residual_in, weight, eps, amax_out, stream=None):
+    """amax_out[0] = max |RMSNorm(x + residual) * weight| (include/rq.h)."""
+    rows, hidden = _rows(x, residual_in)
+    _check(lib().rq_add_rmsnorm_amax(_ptr(x), _ptr(residual_in), _ptr(weight), float(eps),
+                                     _ptr(amax_out), rows, hidden, _dt(x), _stream(stream)))
+
+
+def rq_fp8_scale_from_amax(amax, scale_out, stream=None):
+    _check(lib().rq_fp8_scale_from_amax(_ptr(amax), _ptr(scale_out), _stream(stream)))
+
+
+def rq_nvfp4_global_scale_from_amax(amax, gs_out, stream=None):
+    _check(lib().rq_nvfp4_global_scale_from_amax(_ptr(amax), _ptr(gs_out), _stream(stream)))
+
+
+def _heads(t):
+    """(n_tokens, n_heads, token_stride) of a [T, H, 128] view with dense heads."""
+    if t is None:
+        return 0, 0, 0
+    if t.dim() != 3 or t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+        raise ValueError("q / k must be [tokens, heads, head_dim] views with contiguous heads")
+    return t.shape[0], t.shape[1], t.stride(0)
+
+
+def rq_qk_rmsnorm_rope_fp8(q, k, q_weight, k_weight, eps, positions, cos_sin_cache,
+                           q_scale, k_scale, q_out, k_out, stream=None):
+    """Per-head Q/K RMSNorm + NeoX RoPE + FP8 E4M3 store (include/rq.h).
+    q / k may be token-strided views into a fused QKV buffer."""
+    tq, hq, sq = _heads(q)
+    tk, hk, sk = _heads(k)
+    ref = q if q is not None else k
+    if q is not None and k is not None and (tq != tk or q.dtype != k.dtype):
+        raise ValueError("q and k must have the same token count and dtype")
+    head_dim = ref.shape[2]
+    _check(lib().rq_qk_rmsnorm_rope_fp8(
+        _ptr(q), _ptr(k), sq, sk, ref.shape[0], hq, hk, head_dim, _ptr(q_weight),
+        _ptr(k_weight), float(eps), _ptr(positions), _ptr(cos_sin_cache),
+        cos_sin_cache.shape[0], _ptr(q_scale), _ptr(k_scale), _ptr(q_out), _ptr(k_out),
+        _dt(ref), _stream(stream)))
+
+
+def rq_nvfp4_packed_bytes(rows, hidden):
+    return int(lib().rq_nvfp4_packed_bytes(rows, hidden))
+
+
+def rq_nvfp4_scale_bytes(rows, hidden):
+    return int(lib().rq_nvfp4_scale_bytes(rows, hidden))
+
+
+# ---------------------------------------------------------------- conveniences
+def add_rmsnorm_nvfp4(x, residual, weight, eps, global_scale, with_norm_out=False,
+                      in_place=True, stream=None):
+    """Allocate the outputs (torch) and run rq_add_rmsnorm_nvfp4.  Returns
+    (residual_out, q_packed, block_scales, norm_out or None)."""
+    rows, hidden = _rows(x, residual)
+    res_out = residual if in_place else torch.empty_like(x)
+    q = torch.empty((rows, hidden // 2), dtype=torch.uint8, device=x.device)
+    sf = torch.empty((rows, hidden // 16), dtype=torch.uint8, device=x.device)
+    y = torch.empty_like(x) if with_norm_out else None
+    rq_add_rmsnorm_nvfp4(x, residual, res_out, weight, eps, global_scale, q, sf, y, stream)
+    return res_out, q, sf, y
+
+
+def add_rmsnorm_fp8(x, residual, weight, eps, scale, with_norm_out=False, in_place=True,
+                    stream=None):
+    """Allocate the outputs (torch) and run rq_add_rmsnorm_fp8.  Returns
+    (residual_out, q, norm_out or None)."""
+    rows, hidden = _rows(x, residual)
+    res_out = residual if in_place else torch.empty_like(x)
+    q = torch.empty((rows, hidden), dtype=torch.uint8, device=x.device)
+    y = torch.empty_like(x) if with_norm_out else None
+    rq_add_rmsnorm_fp8(x, residual, res_out, weight, eps, scale, q, y, stream)
+    return res_out, q, y

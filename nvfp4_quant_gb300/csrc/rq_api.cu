@@ -1,0 +1,290 @@
+// rq_api.cu -- the C ABI of librq (declared in include/rq.h): argument checks,
+// dispatch by dtype, launch, status codes.  Every check runs before the first
+// CUDA call, so a rejected call touches neither the device nor the stream.
+#include "rq.h"
+#include "rq_launch.h"
+
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sms[kMaxDevices];
+
+rq_status cuda_status(cudaError_t e)
+{
+    if (e == cudaSuccess) return RQ_OK;
+    std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s", cudaGetErrorName(e),
+                  cudaGetErrorString(e));
+    return RQ_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+struct Span {
+    uintptr_t lo, hi;  // [lo, hi); empty when lo == hi
+};
+
+Span span(const void *p, int64_t bytes)
+{
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    return Span{a, a + (uintptr_t)(p ? bytes : 0)};
+}
+
+bool overlap(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
+
+// true if any output overlaps another output or any input; `allow` names one
+// (output, input) pair that may coincide exactly (the in-place residual).
+bool bad_alias(const Span *outs, int n_out, const Span *ins, int n_in, int allow_out = -1,
+               int allow_in = -1)
+{
+    for (int i = 0; i < n_out; ++i) {
+        for (int j = i + 1; j < n_out; ++j)
+            if (overlap(outs[i], outs[j])) return true;
+        for (int j = 0; j < n_in; ++j) {
+            if (!overlap(outs[i], ins[j])) continue;
+            if (i == allow_out && j == allow_in && outs[i].lo == ins[j].lo && outs[i].hi == ins[j].hi)
+                continue;
+            return true;
+        }
+    }
+    return false;
+}
+
+rq_status check_rows(int64_t rows, int64_t hidden, int dt)
+{
+    if (dt != RQ_BF16 && dt != RQ_FP16) return RQ_ERR_DTYPE;
+    if (rows < 0 || hidden <= 0 || hidden % 16 != 0) return RQ_ERR_SHAPE;
+    if (hidden > RQ_MAX_HIDDEN) return RQ_ERR_UNSUPPORTED;
+    if (rows > (int64_t)1 << 40) return RQ_ERR_SHAPE;
+    return RQ_OK;
+}
+
+rq::NormQuantParams make_params(const void *x, const void *res_in, void *res_out, const void *w,
+                                float eps, const float *scale, uint8_t *q, uint8_t *sf,
+                                void *norm_out, float *amax, int64_t rows, int64_t hidden)
+{
+    rq::NormQuantParams p;
+    p.x = x;
+    p.res_in = res_in;
+    p.res_out = res_out;
+    p.w = w;
+    p.norm_out = norm_out;
+    p.q = q;
+    p.sf = sf;
+    p.scale = scale;
+    p.amax = amax;
+    p.eps = eps;
+    p.rows = rows;
+    p.hidden = (int)hidden;
+    p.nvec = (int)(hidden / 8);
+    return p;
+}
+
+template <int MODE>
+rq_status launch_rows(const rq::NormQuantParams &p, rq_dtype dt, rq_stream_t stream)
+{
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = dt == RQ_BF16 ? rq::launch_add_rmsnorm<rq::BF16, MODE>(p, s)
+                                  : rq::launch_add_rmsnorm<rq::FP16, MODE>(p, s);
+    return cuda_status(e);
+}
+
+}  // namespace
+
+namespace rq {
+int device_sms(int dev)
+{
+    int v = dev >= 0 && dev < kMaxDevices ? g_sms[dev].load(std::memory_order_relaxed) : 0;
+    if (v > 0) return v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v < 1) v = 1;
+    if (dev >= 0 && dev < kMaxDevices) g_sms[dev].store(v, std::memory_order_relaxed);
+    return v;
+}
+}  // namespace rq
+
+extern "C" {
+
+rq_status rq_add_rmsnorm_fp8(const void *x, const void *residual_in, void *residual_out,
+                             const void *weight, float eps, const float *d_scale, uint8_t *q_out,
+                             void *norm_out, int64_t rows, int64_t hidden, rq_dtype dt,
+                             rq_stream_t stream)
+{
+    rq_status st = check_rows(rows, hidden, dt);
+    if (st != RQ_OK) return st;
+    if (!x || !residual_in || !residual_out || !weight || !d_scale || !q_out) return RQ_ERR_NULL;
+    if (!aligned16(x) || !aligned16(residual_in) || !aligned16(residual_out) || !aligned16(weight) ||
+        !aligned16(q_out) || (norm_out && !aligned16(norm_out)) || !aligned4(d_scale))
+        return RQ_ERR_MISALIGNED;
+    const int64_t tb = rows * hidden * 2;
+    const Span ins[] = {span(x, tb), span(residual_in, tb), span(weight, hidden * 2), span(d_scale, 4)};
+    const Span outs[] = {span(residual_out, tb), span(norm_out, tb), span(q_out, rows * hidden)};
+    if (bad_alias(outs, 3, ins, 4, 0, 1)) return RQ_ERR_ALIAS;
+    if (rows == 0) return RQ_OK;
+    auto p = make_params(x, residual_in, residual_out, weight, eps, d_scale, q_out, nullptr, norm_out,
+                         nullptr, rows, hidden);
+    return launch_rows<rq::MODE_FP8>(p, dt, stream);
+}
+
+rq_status rq_add_rmsnorm_nvfp4(const void *x, const void *residual_in, void *residual_out,
+                               const void *weight, float eps, const float *d_global_scale,
+                               uint8_t *q_packed, uint8_t *block_scales, void *norm_out,
+                               int64_t rows, int64_t hidden, rq_dtype dt, rq_stream_t stream)
+{
+    rq_status st = check_rows(rows, hidden, dt);
+    if (st != RQ_OK) return st;
+    if (!x || !residual_in || !residual_out || !weight || !d_global_scale || !q_packed ||
+        !block_scales)
+        return RQ_ERR_NULL;
+    if (!aligned16(x) || !aligned16(residual_in) || !aligned16(residual_out) || !aligned16(weight) ||
+        !aligned16(q_packed) || !aligned16(block_scales) || (norm_out && !aligned16(norm_out)) ||
+        !aligned4(d_global_scale))
+        return RQ_ERR_MISALIGNED;
+    const int64_t tb = rows * hidden * 2;
+    const Span ins[] = {span(x, tb), span(residual_in, tb), span(weight, hidden * 2),
+                        span(d_global_scale, 4)};
+    const Span outs[] = {span(residual_out, tb), span(norm_out, tb), span(q_packed, rows * hidden / 2),
+                         span(block_scales, rows * hidden / 16)};
+    if (bad_alias(outs, 4, ins, 4, 0, 1)) return RQ_ERR_ALIAS;
+    if (rows == 0) return RQ_OK;
+    auto p = make_params(x, residual_in, residual_out, weight, eps, d_global_scale, q_packed,
+                         block_scales, norm_out, nullptr, rows, hidden);
+    return launch_rows<rq::MODE_NVFP4>(p, dt, stream);
+}
+
+rq_status rq_add_rmsnorm_amax(const void *x, const void *residual_in, const void *weight, float eps,
+                              float *d_amax, int64_t rows, int64_t hidden, rq_dtype dt,
+                              rq_stream_t stream)
+{
+    rq_status st = check_rows(rows, hidden, dt);
+    if (st != RQ_OK) return st;
+    if (!x || !residual_in || !weight || !d_amax) return RQ_ERR_NULL;
+    if (!aligned16(x) || !aligned16(residual_in) || !aligned16(weight) || !aligned4(d_amax))
+        return RQ_ERR_MISALIGNED;
+    const int64_t tb = rows * hidden * 2;
+    const Span ins[] = {span(x, tb), span(residual_in, tb), span(weight, hidden * 2)};
+    const Span outs[] = {span(d_amax, 4)};
+    if (bad_alias(outs, 1, ins, 3)) return RQ_ERR_ALIAS;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    st = cuda_status(cudaMemsetAsync(d_amax, 0, sizeof(float), s));
+    if (st != RQ_OK || rows == 0) return st;
+    auto p = make_params(x, residual_in, nullptr, weight, eps, nullptr, nullptr, nullptr, nullptr,
+                         d_amax, rows, hidden);
+    return launch_rows<rq::MODE_AMAX>(p, dt, stream);
+}
+
+static rq_status scale_from_amax(const float *d_amax, float *d_out, int nvfp4, rq_stream_t stream)
+{
+    if (!d_amax || !d_out) return RQ_ERR_NULL;
+    if (!aligned4(d_amax) || !aligned4(d_out)) return RQ_ERR_MISALIGNED;
+    return cuda_status(
+        rq::launch_scale_from_amax(d_amax, d_out, nvfp4, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+rq_status rq_fp8_scale_from_amax(const float *d_amax, float *d_scale, rq_stream_t stream)
+{
+    return scale_from_amax(d_amax, d_scale, 0, stream);
+}
+
+rq_status rq_nvfp4_global_scale_from_amax(const float *d_amax, float *d_gs, rq_stream_t stream)
+{
+    return scale_from_amax(d_amax, d_gs, 1, stream);
+}
+
+rq_status rq_qk_rmsnorm_rope_fp8(const void *q, const void *k, int64_t q_token_stride,
+                                 int64_t k_token_stride, int64_t n_tokens, int n_q_heads,
+                                 int n_k_heads, int head_dim, const void *q_weight,
+                                 const void *k_weight, float eps, const int32_t *positions,
+                                 const float *cos_sin_cache, int64_t max_pos,
+                                 const float *d_q_scale, const float *d_k_scale, uint8_t *q_out,
+                                 uint8_t *k_out, rq_dtype dt, rq_stream_t stream)
+{
+    if (dt != RQ_BF16 && dt != RQ_FP16) return RQ_ERR_DTYPE;
+    if (n_tokens < 0 || n_q_heads < 0 || n_k_heads < 0 || max_pos < 1 || n_tokens > (int64_t)1 << 36)
+        return RQ_ERR_SHAPE;
+    if (head_dim != RQ_QK_HEAD_DIM) return RQ_ERR_UNSUPPORTED;
+    const bool has_q = n_q_heads > 0, has_k = n_k_heads > 0;
+    if (has_q && (q_token_stride < (int64_t)n_q_heads * head_dim || q_token_stride % 8 != 0))
+        return q_token_stride % 8 != 0 ? RQ_ERR_MISALIGNED : RQ_ERR_SHAPE;
+    if (has_k && (k_token_stride < (int64_t)n_k_heads * head_dim || k_token_stride % 8 != 0))
+        return k_token_stride % 8 != 0 ? RQ_ERR_MISALIGNED : RQ_ERR_SHAPE;
+    if (!positions || !cos_sin_cache) return RQ_ERR_NULL;
+    if (has_q && (!q || !q_weight || !d_q_scale || !q_out)) return RQ_ERR_NULL;
+    if (has_k && (!k || !k_weight || !d_k_scale || !k_out)) return RQ_ERR_NULL;
+    if (!aligned16(cos_sin_cache) || !aligned4(positions)) return RQ_ERR_MISALIGNED;
+    if (has_q && (!aligned16(q) || !aligned16(q_weight) || !aligned16(q_out) || !aligned4(d_q_scale)))
+        return RQ_ERR_MISALIGNED;
+    if (has_k && (!aligned16(k) || !aligned16(k_weight) || !aligned16(k_out) || !aligned4(d_k_scale)))
+        return RQ_ERR_MISALIGNED;
+    // input extents: the last token's heads end before (T-1)*stride + H*D
+    const int64_t qin = has_q && n_tokens > 0 ? ((n_tokens - 1) * q_token_stride + (int64_t)n_q_heads * head_dim) * 2 : 0;
+    const int64_t kin = has_k && n_tokens > 0 ? ((n_tokens - 1) * k_token_stride + (int64_t)n_k_heads * head_dim) * 2 : 0;
+    const Span ins[] = {span(has_q ? q : nullptr, qin), span(has_k ? k : nullptr, kin),
+                        span(has_q ? q_weight : nullptr, head_dim * 2),
+                        span(has_k ? k_weight : nullptr, head_dim * 2), span(positions, n_tokens * 4),
+                        span(cos_sin_cache, max_pos * head_dim * 4),
+                        span(has_q ? d_q_scale : nullptr, 4), span(has_k ? d_k_scale : nullptr, 4)};
+    const Span outs[] = {span(has_q ? q_out : nullptr, n_tokens * n_q_heads * (int64_t)head_dim),
+                         span(has_k ? k_out : nullptr, n_tokens * n_k_heads * (int64_t)head_dim)};
+    if (bad_alias(outs, 2, ins, 8)) return RQ_ERR_ALIAS;
+    if (n_tokens == 0 || (!has_q && !has_k)) return RQ_OK;
+
+    rq::QKParams p;
+    p.q = q;
+    p.k = k;
+    p.q_stride = q_token_stride;
+    p.k_stride = k_token_stride;
+    p.n_tokens = n_tokens;
+    p.hq = n_q_heads;
+    p.hk = n_k_heads;
+    p.qw = q_weight;
+    p.kw = k_weight;
+    p.eps = eps;
+    p.pos = positions;
+    p.cos_sin = cos_sin_cache;
+    p.max_pos = max_pos;
+    p.q_scale = d_q_scale;
+    p.k_scale = d_k_scale;
+    p.q_out = q_out;
+    p.k_out = k_out;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = dt == RQ_BF16 ? rq::launch_qk_rmsnorm_rope_fp8<rq::BF16>(p, s)
+                                  : rq::launch_qk_rmsnorm_rope_fp8<rq::FP16>(p, s);
+    return cuda_status(e);
+}
+
+size_t rq_nvfp4_packed_bytes(int64_t rows, int64_t hidden)
+{
+    return rows > 0 && hidden > 0 ? (size_t)rows * (size_t)hidden / 2 : 0;
+}
+
+size_t rq_nvfp4_scale_bytes(int64_t rows, int64_t hidden)
+{
+    return rows > 0 && hidden > 0 ? (size_t)rows * (size_t)(hidden / 16) : 0;
+}
+
+const char *rq_status_string(rq_status status)
+{
+    switch (status) {
+    case RQ_OK: return "RQ_OK";
+    case RQ_ERR_NULL: return "RQ_ERR_NULL: a required pointer is NULL";
+    case RQ_ERR_SHAPE: return "RQ_ERR_SHAPE: invalid rows, hidden, stride or head count";
+    case RQ_ERR_DTYPE: return "RQ_ERR_DTYPE: dtype must be RQ_BF16 or RQ_FP16";
+    case RQ_ERR_MISALIGNED: return "RQ_ERR_MISALIGNED: tensors need 16-byte alignment, scalars 4";
+    case RQ_ERR_ALIAS: return "RQ_ERR_ALIAS: an output overlaps another argument";
+    case RQ_ERR_UNSUPPORTED: return "RQ_ERR_UNSUPPORTED: hidden above the maximum or head_dim != 128";
+    case RQ_ERR_CUDA: return "RQ_ERR_CUDA: the CUDA runtime reported an error";
+    }
+    return "unknown rq_status";
+}
+
+const char *rq_last_error(void) { return g_last_error; }
+
+int rq_version(void) { return 100; }
+
+}  // extern "C"

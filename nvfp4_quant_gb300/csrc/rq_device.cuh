@@ -1,0 +1,197 @@
+// rq_device.cuh -- device helpers shared by the librq kernels: 128-bit memory
+// access with cache hints, dtype packing, FP8/FP4 conversions and group
+// reductions.  sm_103a only.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rq {
+
+// ---------------------------------------------------------------- memory
+// Streaming 16-byte load of data read exactly once (x, residual): no L1
+// allocation.  Plain (coherent) load, so it is also correct for the residual
+// buffer that the same thread overwrites in place afterwards.
+__device__ __forceinline__ uint4 ld_stream16(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// 16-byte load of data shared by many rows (weight, RoPE table): cached.
+__device__ __forceinline__ uint4 ld_keep16(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float ld_f32(const float *p)
+{
+    float v;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ int ld_s32(const int32_t *p)
+{
+    int v;
+    asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st16(void *p, uint4 v)
+{
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+__device__ __forceinline__ void st8(void *p, uint32_t lo, uint32_t hi)
+{
+    asm volatile("st.global.v2.u32 [%0], {%1, %2};" :: "l"(p), "r"(lo), "r"(hi) : "memory");
+}
+
+__device__ __forceinline__ void st4(void *p, uint32_t v)
+{
+    asm volatile("st.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st1(void *p, uint32_t v)
+{
+    asm volatile("st.global.u8 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
+// ---------------------------------------------------------------- dtypes
+// A 32-bit word holds two 16-bit elements, the lower-addressed one in the
+// low half.  Unpacking is exact; packing rounds to nearest even.
+struct BF16 {
+    static __device__ __forceinline__ float lo(uint32_t u) { return __uint_as_float(u << 16); }
+    static __device__ __forceinline__ float hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+    static __device__ __forceinline__ uint32_t pack(float lo_v, float hi_v)
+    {
+        uint32_t d;
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi_v), "f"(lo_v));
+        return d;
+    }
+};
+
+struct FP16 {
+    static __device__ __forceinline__ float lo(uint32_t u)
+    {
+        float f;
+        asm("{ .reg .b16 l, h; mov.b32 {l, h}, %1; cvt.f32.f16 %0, l; }" : "=f"(f) : "r"(u));
+        return f;
+    }
+    static __device__ __forceinline__ float hi(uint32_t u)
+    {
+        float f;
+        asm("{ .reg .b16 l, h; mov.b32 {l, h}, %1; cvt.f32.f16 %0, h; }" : "=f"(f) : "r"(u));
+        return f;
+    }
+    static __device__ __forceinline__ uint32_t pack(float lo_v, float hi_v)
+    {
+        uint32_t d;
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi_v), "f"(lo_v));
+        return d;
+    }
+};
+
+// 8 elements of one 16-byte vector as floats
+template <typename DT>
+__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8])
+{
+    f[0] = DT::lo(v.x); f[1] = DT::hi(v.x);
+    f[2] = DT::lo(v.y); f[3] = DT::hi(v.y);
+    f[4] = DT::lo(v.z); f[5] = DT::hi(v.z);
+    f[6] = DT::lo(v.w); f[7] = DT::hi(v.w);
+}
+
+template <typename DT>
+__device__ __forceinline__ uint4 pack8(const float (&f)[8])
+{
+    uint4 v;
+    v.x = DT::pack(f[0], f[1]);
+    v.y = DT::pack(f[2], f[3]);
+    v.z = DT::pack(f[4], f[5]);
+    v.w = DT::pack(f[6], f[7]);
+    return v;
+}
+
+// ---------------------------------------------------------------- FP8 / FP4
+// Two fp32 -> two E4M3 bytes (round to nearest even, satfinite); the first
+// argument goes to the lower byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo_v, float hi_v)
+{
+    uint32_t d;
+    asm("{ .reg .b16 t; cvt.rn.satfinite.e4m3x2.f32 t, %1, %2; cvt.u32.u16 %0, t; }"
+        : "=r"(d) : "f"(hi_v), "f"(lo_v));
+    return d;
+}
+
+// Eight fp32 -> eight E4M3 bytes, element 0 in the lowest byte of .x.
+__device__ __forceinline__ uint2 e4m3x8(const float (&v)[8])
+{
+    uint2 r;
+    r.x = e4m3x2(v[0], v[1]) | (e4m3x2(v[2], v[3]) << 16);
+    r.y = e4m3x2(v[4], v[5]) | (e4m3x2(v[6], v[7]) << 16);
+    return r;
+}
+
+// Eight fp32 -> eight E2M1 nibbles packed in 32 bits, element 0 in the
+// lowest nibble (round to nearest even, satfinite).
+__device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8])
+{
+    uint32_t d;
+    asm("{\n"
+        " .reg .b8 b0, b1, b2, b3;\n"
+        " cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+        " cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+        " cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+        " cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+        " mov.b32 %0, {b0, b1, b2, b3};\n"
+        "}"
+        : "=r"(d)
+        : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]),
+          "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+    return d;
+}
+
+// Value of an E4M3 byte (exact; the byte comes from e4m3x2, so never NaN).
+__device__ __forceinline__ float e4m3_value(uint32_t byte)
+{
+    float f;
+    asm("{ .reg .b16 c; .reg .b32 h2; .reg .b16 lo, hi;\n"
+        " cvt.u16.u32 c, %1;\n"
+        " cvt.rn.f16x2.e4m3x2 h2, c;\n"
+        " mov.b32 {lo, hi}, h2;\n"
+        " cvt.f32.f16 %0, lo; }"
+        : "=f"(f) : "r"(byte));
+    return f;
+}
+
+// ---------------------------------------------------------------- reductions
+// Sum over aligned groups of G lanes (G a power of two <= 32) of one warp;
+// every lane of the group receives the same result, summed in the same
+// order.
+template <int G>
+__device__ __forceinline__ float group_sum(float v)
+{
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+template <int G>
+__device__ __forceinline__ float group_max(float v)
+{
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+}  // namespace rq

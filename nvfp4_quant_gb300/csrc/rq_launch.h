@@ -1,0 +1,61 @@
+// rq_launch.h -- host-side launch interface between the C ABI (rq_api.cu) and
+// the kernel translation units.  Internal to librq.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rq {
+
+struct BF16;
+struct FP16;
+
+struct NormQuantParams {
+    const void *x;
+    const void *res_in;
+    void *res_out;
+    const void *w;
+    void *norm_out;      // may be null
+    uint8_t *q;          // FP8 codes [rows, H] or NVFP4 packed [rows, H/2]
+    uint8_t *sf;         // NVFP4 block scales [rows, H/16]
+    const float *scale;  // FP8 dequant scale or NVFP4 global scale
+    float *amax;         // amax-mode output
+    float eps;
+    int64_t rows;
+    int hidden;
+    int nvec;            // hidden / 8
+};
+
+struct QKParams {
+    const void *q;
+    const void *k;
+    int64_t q_stride;    // elements between tokens
+    int64_t k_stride;
+    int64_t n_tokens;
+    int hq, hk;
+    const void *qw;
+    const void *kw;
+    float eps;
+    const int32_t *pos;
+    const float *cos_sin;
+    int64_t max_pos;
+    const float *q_scale;
+    const float *k_scale;
+    uint8_t *q_out;
+    uint8_t *k_out;
+};
+
+enum QuantMode { MODE_FP8 = 0, MODE_NVFP4 = 1, MODE_AMAX = 2 };
+
+// SM count of device `dev` (cached).
+int device_sms(int dev);
+
+template <typename DT, int MODE>
+cudaError_t launch_add_rmsnorm(const NormQuantParams &p, cudaStream_t stream);
+
+template <typename DT>
+cudaError_t launch_qk_rmsnorm_rope_fp8(const QKParams &p, cudaStream_t stream);
+
+cudaError_t launch_scale_from_amax(const float *amax, float *out, int nvfp4, cudaStream_t stream);
+
+}  // namespace rq

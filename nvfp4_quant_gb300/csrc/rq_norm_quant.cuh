@@ -1,0 +1,189 @@
+// rq_norm_quant.cuh -- the fused residual add + RMSNorm (+ norm output) +
+// FP8 / NVFP4 kernel, and its amax-calibration variant.
+//
+// Prior art: "[Performance]: Fuse local NVFP4 tail after NCCL fallback"
+// (TensorRT-LLM issue 17900), Proposal: one launch for residual + RMSNorm +
+// NVFP4 instead of separate kernels; "Add NanoJet backend for AutoDeploy
+// prefill-only FP8 inference", Description: RMSNorm with FP8 quantisation in
+// the epilogue.  The design below is ours, for GB300.
+//
+// Work mapping.  A row of `hidden` elements is split into nvec = hidden / 8
+// vectors of 16 bytes.  A row group of G threads owns one row; thread t of the
+// group holds vectors t, t + G, ..., t + (VPT-1) G, so each warp-wide access
+// touches consecutive 16-byte vectors (fully coalesced) and the two vectors
+// of one 16-element NVFP4 block sit in neighbouring lanes.  G <= 32 packs
+// 32 / G rows into a warp; G > 32 spans warps of one CTA.  The grid is
+// persistent: each CTA walks row groups with a grid stride, keeping the
+// weight in registers for all its rows.
+//
+// Per row: 16-byte loads of x and residual -> fp32 add -> round to the dtype
+// -> store residual' -> fp32 sum of squares of the rounded values (shuffle
+// tree, then shared memory across warps) -> rstd with IEEE div / sqrt ->
+// y = dt((s * rstd) * w) -> optional norm_out store -> quantise from the
+// rounded y.
+#pragma once
+
+#include "rq_device.cuh"
+#include "rq_launch.h"
+
+namespace rq {
+
+template <int G>
+struct GroupShape {
+    static constexpr int kBlock = G >= 128 ? G : 128;    // threads per CTA
+    static constexpr int kRowsPerCta = kBlock / G;
+    static constexpr int kWarps = kBlock / 32;
+    static constexpr int kWarpsPerGroup = G > 32 ? G / 32 : 1;
+};
+
+template <typename DT, int G, int VPT, int MODE>
+__global__ void __launch_bounds__(GroupShape<G>::kBlock)
+add_rmsnorm_quant_kernel(const NormQuantParams p)
+{
+    using S = GroupShape<G>;
+    const int tid = threadIdx.x;
+    const int t = tid % G;
+    const int grp = tid / G;
+    const int nvec = p.nvec;
+    const int64_t H = p.hidden;
+
+    __shared__ float red[2][S::kWarps];
+
+    // weight vectors of this thread, kept for every row it processes
+    uint4 wv[VPT];
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int k = j * G + t;
+        wv[j] = k < nvec ? ld_keep16(static_cast<const uint8_t *>(p.w) + (int64_t)k * 16)
+                         : make_uint4(0, 0, 0, 0);
+    }
+    const float scale = MODE == MODE_AMAX ? 0.0f : ld_f32(p.scale);
+    const bool sf_words = (p.hidden % 64) == 0;  // 4 block scales per 32-bit store
+    float amax_acc = 0.0f;
+    int parity = 0;
+
+    for (int64_t base = (int64_t)blockIdx.x * S::kRowsPerCta; base < p.rows;
+         base += (int64_t)gridDim.x * S::kRowsPerCta) {
+        const int64_t row = base + grp;
+        const bool row_ok = row < p.rows;
+        const uint8_t *xrow = static_cast<const uint8_t *>(p.x) + row * H * 2;
+        const uint8_t *rrow = static_cast<const uint8_t *>(p.res_in) + row * H * 2;
+
+        // ---- loads: all of this thread's vectors before any use
+        uint4 xv[VPT], sv[VPT];
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int k = j * G + t;
+            if (row_ok && k < nvec) {
+                xv[j] = ld_stream16(xrow + (int64_t)k * 16);
+                sv[j] = ld_stream16(rrow + (int64_t)k * 16);
+            } else {
+                xv[j] = make_uint4(0, 0, 0, 0);
+                sv[j] = make_uint4(0, 0, 0, 0);
+            }
+        }
+
+        // ---- residual' = dt(x + r), stored; sum of squares of the rounded values
+        float ss = 0.0f;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            float a[8], b[8];
+            unpack8<DT>(xv[j], a);
+            unpack8<DT>(sv[j], b);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) a[e] = __fadd_rn(a[e], b[e]);
+            sv[j] = pack8<DT>(a);
+            unpack8<DT>(sv[j], a);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ss = __fmaf_rn(a[e], a[e], ss);  // squares are exact
+            const int k = j * G + t;
+            if (MODE != MODE_AMAX && row_ok && k < nvec)
+                st16(static_cast<uint8_t *>(p.res_out) + (row * H + (int64_t)k * 8) * 2, sv[j]);
+        }
+
+        // ---- row reduction
+        if (G <= 32) {
+            ss = group_sum<(G <= 32 ? G : 32)>(ss);
+        } else {
+            ss = group_sum<32>(ss);
+            if ((tid & 31) == 0) red[parity][tid >> 5] = ss;
+            __syncthreads();
+            const int w0 = grp * S::kWarpsPerGroup;
+            ss = 0.0f;
+#pragma unroll
+            for (int i = 0; i < S::kWarpsPerGroup; ++i) ss = __fadd_rn(ss, red[parity][w0 + i]);
+            parity ^= 1;
+        }
+        const float ms = __fdiv_rn(ss, (float)p.hidden);
+        const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, p.eps)));
+
+        // ---- normalise, store, quantise
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int k = j * G + t;
+            const bool ok = row_ok && k < nvec;
+            float s[8], w[8], y[8];
+            unpack8<DT>(sv[j], s);
+            unpack8<DT>(wv[j], w);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) y[e] = __fmul_rn(__fmul_rn(s[e], rstd), w[e]);
+            const uint4 yv = pack8<DT>(y);
+            if (MODE != MODE_AMAX && p.norm_out != nullptr && ok)
+                st16(static_cast<uint8_t *>(p.norm_out) + (row * H + (int64_t)k * 8) * 2, yv);
+            unpack8<DT>(yv, y);  // quantise from the dtype-rounded norm output
+
+            if (MODE == MODE_FP8) {
+                float v[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] = __fdiv_rn(y[e], scale);
+                const uint2 c = e4m3x8(v);
+                if (ok) st8(p.q + row * H + (int64_t)k * 8, c.x, c.y);
+            } else if (MODE == MODE_NVFP4) {
+                float m = 0.0f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(y[e]));
+                const float a = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));  // 16-element block
+                const float t2 = __fdiv_rn(__fmul_rn(scale, a), 6.0f);
+                const uint32_t sfc = e4m3x2(t2, 0.0f) & 0xFFu;
+                const float sfv = e4m3_value(sfc);
+                const float enc = sfv == 0.0f ? 0.0f : __fdiv_rn(scale, sfv);
+                float v[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(y[e], enc);
+                const uint32_t codes = e2m1x8(v);
+                if (ok) st4(p.q + row * (H / 2) + (int64_t)k * 4, codes);
+                // block scales: lane t (k even) owns block k/2
+                uint8_t *sfrow = p.sf + row * (H / 16);
+                if (sf_words) {
+                    const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, sfc, 2);
+                    const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sfc, 4);
+                    const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sfc, 6);
+                    if (ok && (k & 7) == 0) st4(sfrow + k / 2, sfc | (b1 << 8) | (b2 << 16) | (b3 << 24));
+                } else if (ok && (k & 1) == 0) {
+                    st1(sfrow + k / 2, sfc);
+                }
+            } else {  // MODE_AMAX
+                if (ok) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) amax_acc = fmaxf(amax_acc, fabsf(y[e]));
+                }
+            }
+        }
+    }
+
+    if (MODE == MODE_AMAX) {
+        // block maximum, then one atomic per CTA on the float's bit pattern
+        // (non-negative floats order like their unsigned bits)
+        float m = group_max<32>(amax_acc);
+        __syncthreads();
+        if ((tid & 31) == 0) red[0][tid >> 5] = m;
+        __syncthreads();
+        if (tid == 0) {
+            float r = 0.0f;
+            for (int i = 0; i < S::kWarps; ++i) r = fmaxf(r, red[0][i]);
+            atomicMax(reinterpret_cast<unsigned int *>(p.amax), __float_as_uint(r));
+        }
+    }
+}
+
+}  // namespace rq

@@ -1,0 +1,143 @@
+"""The C ABI without a GPU: the library loads, exports every entry point that
+include/rq.h declares, and rejects bad arguments with the documented status
+before any CUDA call (the pointers below are never dereferenced)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import nvfp4_quant_gb300 as rq
+from nvfp4_quant_gb300 import build as rq_build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "rq.h")
+OK, NULL, SHAPE, DTYPE, MISAL, ALIAS, UNSUP = 0, 1, 2, 3, 4, 5, 6
+
+
+@pytest.fixture(scope="module")
+def L():
+    rq_build.build()
+    return rq.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert "rq_add_rmsnorm_nvfp4" in names and len(names) >= 10
+    for n in names:
+        assert hasattr(L, n), n
+        assert n in rq.SIGNATURES, "binding lacks " + n
+
+
+def test_status_strings_and_sizes(L):
+    for code in range(8):
+        assert L.rq_status_string(code).decode().startswith(rq.STATUS[code])
+    assert rq.rq_nvfp4_packed_bytes(64, 8192) == 64 * 4096
+    assert rq.rq_nvfp4_scale_bytes(64, 8192) == 64 * 512
+    assert rq.rq_nvfp4_scale_bytes(0, 8192) == 0
+    assert L.rq_version() >= 100
+
+
+# distinct, 16-byte aligned fake addresses far apart
+A = {n: 0x10000000 * (i + 1) for i, n in enumerate(
+    ["x", "r", "ro", "w", "s", "q", "sf", "y", "amax", "pos", "cs", "qs", "ks", "qo", "ko", "k"])}
+
+
+def fp8(L, **kw):
+    a = dict(x=A["x"], r=A["r"], ro=A["ro"], w=A["w"], eps=1e-6, s=A["s"], q=A["q"], y=A["y"],
+             rows=16, hidden=128, dt=0)
+    a.update(kw)
+    return L.rq_add_rmsnorm_fp8(a["x"], a["r"], a["ro"], a["w"], a["eps"], a["s"], a["q"], a["y"],
+                                a["rows"], a["hidden"], a["dt"], None)
+
+
+def nvfp4(L, **kw):
+    a = dict(x=A["x"], r=A["r"], ro=A["ro"], w=A["w"], eps=1e-6, s=A["s"], q=A["q"], sf=A["sf"],
+             y=A["y"], rows=16, hidden=128, dt=1)
+    a.update(kw)
+    return L.rq_add_rmsnorm_nvfp4(a["x"], a["r"], a["ro"], a["w"], a["eps"], a["s"], a["q"], a["sf"],
+                                  a["y"], a["rows"], a["hidden"], a["dt"], None)
+
+
+def qk(L, **kw):
+    a = dict(q=A["x"], k=A["k"], qst=16 * 128, kst=8 * 128, T=32, hq=16, hk=8, hd=128, qw=A["w"],
+             kw=A["r"], eps=1e-6, pos=A["pos"], cs=A["cs"], maxp=4096, qs=A["qs"], ks=A["ks"],
+             qo=A["qo"], ko=A["ko"], dt=0)
+    a.update(kw)
+    return L.rq_qk_rmsnorm_rope_fp8(a["q"], a["k"], a["qst"], a["kst"], a["T"], a["hq"], a["hk"],
+                                    a["hd"], a["qw"], a["kw"], a["eps"], a["pos"], a["cs"],
+                                    a["maxp"], a["qs"], a["ks"], a["qo"], a["ko"], a["dt"], None)
+
+
+@pytest.mark.parametrize("call", [fp8, nvfp4])
+def test_row_call_rejections(L, call):
+    assert call(L, rows=0) == OK  # nothing to do, no launch
+    assert call(L, x=None) == NULL
+    assert call(L, w=None) == NULL
+    assert call(L, s=None) == NULL
+    assert call(L, q=None) == NULL
+    assert call(L, rows=-1) == SHAPE
+    assert call(L, hidden=0) == SHAPE
+    assert call(L, hidden=136) == SHAPE  # not a multiple of 16
+    assert call(L, hidden=32768 + 16) == UNSUP
+    assert call(L, dt=2) == DTYPE
+    assert call(L, x=A["x"] + 8) == MISAL
+    assert call(L, q=A["q"] + 4) == MISAL
+    assert call(L, y=A["y"] + 2) == MISAL
+    assert call(L, s=A["s"] + 2) == MISAL
+    # in place residual is allowed, partial overlap is not
+    assert call(L, ro=A["r"], rows=0) == OK
+    assert call(L, ro=A["r"] + 16) == ALIAS
+    assert call(L, ro=A["x"]) == ALIAS
+    assert call(L, y=A["ro"]) == ALIAS
+    assert call(L, q=A["w"]) == ALIAS
+    assert call(L, y=A["s"] - 16) == ALIAS  # norm out covering the scale scalar
+
+
+def test_nvfp4_specific_rejections(L):
+    assert nvfp4(L, sf=None) == NULL
+    assert nvfp4(L, sf=A["sf"] + 1) == MISAL
+    assert nvfp4(L, sf=A["q"] + 16 * 64 - 16) == ALIAS  # scales inside the packed codes
+    assert nvfp4(L, y=None, rows=0) == OK  # norm output is optional
+
+
+def test_amax_rejections(L):
+    f = lambda **kw: L.rq_add_rmsnorm_amax(kw.get("x", A["x"]), kw.get("r", A["r"]), kw.get("w", A["w"]),
+                                           1e-6, kw.get("amax", A["amax"]), kw.get("rows", 4),
+                                           kw.get("hidden", 64), kw.get("dt", 0), None)
+    assert f(amax=None) == NULL
+    assert f(amax=A["amax"] + 2) == MISAL
+    assert f(hidden=8) == SHAPE
+    assert f(amax=A["x"] + 64) == ALIAS
+    assert L.rq_fp8_scale_from_amax(None, A["s"], None) == NULL
+    assert L.rq_nvfp4_global_scale_from_amax(A["amax"], A["s"] + 1, None) == MISAL
+
+
+def test_qk_rejections(L):
+    assert qk(L, T=0) == OK
+    assert qk(L, hd=64) == UNSUP
+    assert qk(L, dt=5) == DTYPE
+    assert qk(L, T=-1) == SHAPE
+    assert qk(L, maxp=0) == SHAPE
+    assert qk(L, qst=15 * 128) == SHAPE  # stride shorter than the heads of a token
+    assert qk(L, qst=16 * 128 + 4) == MISAL
+    assert qk(L, pos=None) == NULL
+    assert qk(L, cs=None) == NULL
+    assert qk(L, qs=None) == NULL
+    assert qk(L, k=None) == NULL
+    assert qk(L, k=None, kw=None, ks=None, ko=None, hk=0, T=0) == OK  # Q only
+    assert qk(L, qo=A["qo"] + 8) == MISAL
+    assert qk(L, ko=A["qo"] + 32 * 16 * 128 - 16) == ALIAS
+    assert qk(L, qo=A["cs"]) == ALIAS
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(rq, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(rq, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        rq.lib()
