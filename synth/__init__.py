@@ -15,13 +15,16 @@ cosine branch on the uniforms (u[2i], u[2i+1]).
 Tensor ids: x = 1, residual = 2, weight = 3, q = 4, k = 5, q weight = 6,
 k weight = 7, outlier mask = 8.
 """
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import torch
 
 GAMMA = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
-_CHUNK = 1 << 22
+_CHUNK = 1 << 20
 
 TID_X, TID_RES, TID_W, TID_Q, TID_K, TID_QW, TID_KW, TID_OUTLIER = 1, 2, 3, 4, 5, 6, 7, 8
 
@@ -40,27 +43,48 @@ def _key(seed, tensor_id):
     return _mix64(np.array([base], np.uint64))[0]
 
 
+def _uniform_chunk(key, start, n):
+    idx = np.arange(start + 1, start + n + 1, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        z = _mix64(key + idx * GAMMA)
+    return ((z >> np.uint64(11)).astype(np.float64) + 1.0) * (2.0 ** -53)
+
+
+def _parallel(n, fn):
+    """Run fn(c0, c1) over chunks of [0, n) on a thread pool (numpy releases
+    the GIL inside its array loops); chunk results do not depend on the pool."""
+    chunks = [(c0, min(n, c0 + _CHUNK)) for c0 in range(0, n, _CHUNK)]
+    if len(chunks) <= 1:
+        for c in chunks:
+            fn(*c)
+        return
+    workers = max(1, min(len(chunks), os.cpu_count() or 1, 32))
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        list(ex.map(lambda c: fn(*c), chunks))
+
+
 def uniform(seed, tensor_id, n, start=0):
     """n uniforms in (0, 1] (float64): elements start .. start+n-1 of the stream."""
     key = _key(seed, tensor_id)
     out = np.empty(n, np.float64)
-    for c0 in range(0, n, _CHUNK):
-        c1 = min(n, c0 + _CHUNK)
-        idx = np.arange(start + c0 + 1, start + c1 + 1, dtype=np.uint64)
-        with np.errstate(over="ignore"):
-            z = _mix64(key + idx * GAMMA)
-        out[c0:c1] = ((z >> np.uint64(11)).astype(np.float64) + 1.0) * (2.0 ** -53)
+
+    def fill(c0, c1):
+        out[c0:c1] = _uniform_chunk(key, start + c0, c1 - c0)
+
+    _parallel(n, fill)
     return out
 
 
 def normal(seed, tensor_id, n):
     """n standard normals (float64), Box-Muller on consecutive uniform pairs."""
+    key = _key(seed, tensor_id)
     out = np.empty(n, np.float64)
-    for c0 in range(0, n, _CHUNK):
-        c1 = min(n, c0 + _CHUNK)
-        u = uniform(seed, tensor_id, 2 * (c1 - c0), start=2 * c0)
-        u1, u2 = u[0::2], u[1::2]
-        out[c0:c1] = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
+
+    def fill(c0, c1):
+        u = _uniform_chunk(key, 2 * c0, 2 * (c1 - c0))
+        out[c0:c1] = np.sqrt(-2.0 * np.log(u[0::2])) * np.cos(2.0 * np.pi * u[1::2])
+
+    _parallel(n, fill)
     return out
 
 
