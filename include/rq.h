@@ -14,8 +14,9 @@
  *    asynchronous: a returned RQ_OK means the launch was accepted.
  *  - Every argument check runs on the host before any CUDA call; a failed
  *    check returns an error status and launches nothing.  Nothing throws
- *    across the ABI.  rows == 0 (or n_tokens == 0) returns RQ_OK and launches
- *    nothing.
+ *    across the ABI.  A call with rows == 0 (or n_tokens == 0) returns RQ_OK
+ *    once its dtype and shape arguments are valid, whatever its pointers
+ *    (empty tensors may have NULL data), and launches nothing.
  *  - Alignment: every tensor pointer must be 16-byte aligned; scalar pointers
  *    4-byte aligned.
  *  - Aliasing: residual_out may equal residual_in exactly (in-place residual
@@ -147,7 +148,8 @@ rq_status rq_qk_rmsnorm_rope_fp8(const void *q, const void *k,
 /*
  * Calibration: d_amax = max over the tensor of |y| (the norm output the
  * fused calls would produce), written to one device fp32.  Nothing else is
- * written.  The call clears d_amax on `stream` first.
+ * written.  The call clears d_amax on `stream` first (so an empty tensor
+ * gives 0; x, residual_in and weight may then be NULL).
  * Source: the per-tensor scales the pages use are derived from the norm
  * output's absolute maximum ("Add AutoDeploy NVFP4 RMSNorm quant fusion",
  * Changes: reference module with input-scale calibration).

@@ -116,7 +116,7 @@ rq_status rq_add_rmsnorm_fp8(const void *x, const void *residual_in, void *resid
                              rq_stream_t stream)
 {
     rq_status st = check_rows(rows, hidden, dt);
-    if (st != RQ_OK) return st;
+    if (st != RQ_OK || rows == 0) return st;
     if (!x || !residual_in || !residual_out || !weight || !d_scale || !q_out) return RQ_ERR_NULL;
     if (!aligned16(x) || !aligned16(residual_in) || !aligned16(residual_out) || !aligned16(weight) ||
         !aligned16(q_out) || (norm_out && !aligned16(norm_out)) || !aligned4(d_scale))
@@ -125,7 +125,6 @@ rq_status rq_add_rmsnorm_fp8(const void *x, const void *residual_in, void *resid
     const Span ins[] = {span(x, tb), span(residual_in, tb), span(weight, hidden * 2), span(d_scale, 4)};
     const Span outs[] = {span(residual_out, tb), span(norm_out, tb), span(q_out, rows * hidden)};
     if (bad_alias(outs, 3, ins, 4, 0, 1)) return RQ_ERR_ALIAS;
-    if (rows == 0) return RQ_OK;
     auto p = make_params(x, residual_in, residual_out, weight, eps, d_scale, q_out, nullptr, norm_out,
                          nullptr, rows, hidden);
     return launch_rows<rq::MODE_FP8>(p, dt, stream);
@@ -137,7 +136,7 @@ rq_status rq_add_rmsnorm_nvfp4(const void *x, const void *residual_in, void *res
                                int64_t rows, int64_t hidden, rq_dtype dt, rq_stream_t stream)
 {
     rq_status st = check_rows(rows, hidden, dt);
-    if (st != RQ_OK) return st;
+    if (st != RQ_OK || rows == 0) return st;
     if (!x || !residual_in || !residual_out || !weight || !d_global_scale || !q_packed ||
         !block_scales)
         return RQ_ERR_NULL;
@@ -151,7 +150,6 @@ rq_status rq_add_rmsnorm_nvfp4(const void *x, const void *residual_in, void *res
     const Span outs[] = {span(residual_out, tb), span(norm_out, tb), span(q_packed, rows * hidden / 2),
                          span(block_scales, rows * hidden / 16)};
     if (bad_alias(outs, 4, ins, 4, 0, 1)) return RQ_ERR_ALIAS;
-    if (rows == 0) return RQ_OK;
     auto p = make_params(x, residual_in, residual_out, weight, eps, d_global_scale, q_packed,
                          block_scales, norm_out, nullptr, rows, hidden);
     return launch_rows<rq::MODE_NVFP4>(p, dt, stream);
@@ -163,8 +161,10 @@ rq_status rq_add_rmsnorm_amax(const void *x, const void *residual_in, const void
 {
     rq_status st = check_rows(rows, hidden, dt);
     if (st != RQ_OK) return st;
-    if (!x || !residual_in || !weight || !d_amax) return RQ_ERR_NULL;
-    if (!aligned16(x) || !aligned16(residual_in) || !aligned16(weight) || !aligned4(d_amax))
+    if (!d_amax) return RQ_ERR_NULL;
+    if (rows > 0 && (!x || !residual_in || !weight)) return RQ_ERR_NULL;
+    if (!aligned4(d_amax) || (rows > 0 && (!aligned16(x) || !aligned16(residual_in) ||
+                                            !aligned16(weight))))
         return RQ_ERR_MISALIGNED;
     const int64_t tb = rows * hidden * 2;
     const Span ins[] = {span(x, tb), span(residual_in, tb), span(weight, hidden * 2)};
@@ -208,6 +208,7 @@ rq_status rq_qk_rmsnorm_rope_fp8(const void *q, const void *k, int64_t q_token_s
     if (n_tokens < 0 || n_q_heads < 0 || n_k_heads < 0 || max_pos < 1 || n_tokens > (int64_t)1 << 36)
         return RQ_ERR_SHAPE;
     if (head_dim != RQ_QK_HEAD_DIM) return RQ_ERR_UNSUPPORTED;
+    if (n_tokens == 0 || (n_q_heads == 0 && n_k_heads == 0)) return RQ_OK;
     const bool has_q = n_q_heads > 0, has_k = n_k_heads > 0;
     if (has_q && (q_token_stride < (int64_t)n_q_heads * head_dim || q_token_stride % 8 != 0))
         return q_token_stride % 8 != 0 ? RQ_ERR_MISALIGNED : RQ_ERR_SHAPE;
@@ -232,7 +233,6 @@ rq_status rq_qk_rmsnorm_rope_fp8(const void *q, const void *k, int64_t q_token_s
     const Span outs[] = {span(has_q ? q_out : nullptr, n_tokens * n_q_heads * (int64_t)head_dim),
                          span(has_k ? k_out : nullptr, n_tokens * n_k_heads * (int64_t)head_dim)};
     if (bad_alias(outs, 2, ins, 8)) return RQ_ERR_ALIAS;
-    if (n_tokens == 0 || (!has_q && !has_k)) return RQ_OK;
 
     rq::QKParams p;
     p.q = q;

@@ -7,14 +7,16 @@
 // (SGLang PR 32975), review thread (norm + RoPE + uniform FP8 store as one
 // kernel epilogue).  The mapping below is ours.
 //
-// Mapping.  One head row (128 elements = 256 bytes) is owned by 16 lanes, 8
-// elements (one 16-byte vector) per lane, so a warp handles two head rows per
-// step.  NeoX RoPE pairs element i with i + 64, i.e. lane l with lane l ^ 8,
-// and both lanes of a pair use the same cos/sin entries (frequencies
-// 8 * (l & 7) .. + 7).  The sum of squares is a 16-lane shuffle tree; the
-// rounded normalised values are exchanged with one 4-word shuffle.  The grid
-// is persistent and walks head rows token-major, so the cos/sin row of a
-// token is reused from L1 by all its heads.
+// Mapping.  One warp per token (grid-stride over tokens).  A head row (128
+// elements = 256 bytes) is owned by 16 lanes, 8 elements (one 16-byte vector)
+// per lane: lanes 0-15 take the even heads of the token, lanes 16-31 the odd
+// ones.  NeoX RoPE pairs element i with i + 64, i.e. lane l with lane l ^ 8,
+// and both lanes of a pair use the same frequencies 8 * (l & 7) .. + 7, so
+// each lane loads its 8 cos and 8 sin values once per token and keeps them in
+// registers for every head.  Heads are processed kPairs pairs at a time, which
+// keeps kPairs 16-byte loads per lane in flight.  The sum of squares is a
+// 16-lane shuffle tree; the rounded normalised values are exchanged with one
+// 4-word shuffle.
 #include "rq_device.cuh"
 #include "rq_launch.h"
 
@@ -24,17 +26,17 @@ namespace rq {
 
 constexpr int kQKBlock = 256;
 constexpr int kHeadDim = 128;
+constexpr int kPairs = 4;  // head pairs per step: 8 heads, 4 loads in flight per lane
 
 template <typename DT>
-__global__ void __launch_bounds__(kQKBlock)
+__global__ void __launch_bounds__(kQKBlock, 2)
 qk_rmsnorm_rope_fp8_kernel(const QKParams p)
 {
     const int lane16 = threadIdx.x & 15;
-    const int half = (threadIdx.x >> 4) & 1;            // which head row of the warp
+    const int half = (threadIdx.x >> 4) & 1;            // even or odd heads
     const bool upper = lane16 >= 8;                     // holds elements 64..127
     const int rot = (lane16 & 7) * 8;                   // first frequency of this lane
     const int heads = p.hq + p.hk;
-    const int64_t nrows = p.n_tokens * heads;
     const int64_t warp0 = ((int64_t)blockIdx.x * kQKBlock + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * kQKBlock) >> 5;
 
@@ -45,72 +47,75 @@ qk_rmsnorm_rope_fp8_kernel(const QKParams p)
     const float qscale = p.hq > 0 ? ld_f32(p.q_scale) : 1.0f;
     const float kscale = p.hk > 0 ? ld_f32(p.k_scale) : 1.0f;
 
-    for (int64_t wi = warp0; 2 * wi < nrows; wi += nwarps) {
-        const int64_t hr = 2 * wi + half;
-        const bool ok = hr < nrows;
-        const int64_t tok = ok ? hr / heads : 0;
-        const int h = ok ? (int)(hr - tok * heads) : 0;
-        const bool is_q = h < p.hq;
-
-        const uint8_t *src = is_q
-            ? static_cast<const uint8_t *>(p.q) + (tok * p.q_stride + (int64_t)h * kHeadDim) * 2
-            : static_cast<const uint8_t *>(p.k) + (tok * p.k_stride + (int64_t)(h - p.hq) * kHeadDim) * 2;
-        const uint4 xv = ok ? ld_stream16(src + lane16 * 16) : make_uint4(0, 0, 0, 0);
-
-        int pos = ok ? ld_s32(p.pos + tok) : 0;
+    for (int64_t tok = warp0; tok < p.n_tokens; tok += nwarps) {
+        int pos = ld_s32(p.pos + tok);
         pos = pos < 0 ? 0 : (pos >= p.max_pos ? (int)(p.max_pos - 1) : pos);
         const uint8_t *cs = reinterpret_cast<const uint8_t *>(p.cos_sin + (int64_t)pos * kHeadDim);
         const uint4 c0 = ld_keep16(cs + rot * 4), c1 = ld_keep16(cs + rot * 4 + 16);
         const uint4 s0 = ld_keep16(cs + (64 + rot) * 4), s1 = ld_keep16(cs + (64 + rot) * 4 + 16);
-
-        // RMSNorm over the 16 lanes of the head row
-        float x[8];
-        unpack8<DT>(xv, x);
-        float ss = 0.0f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) ss = __fmaf_rn(x[e], x[e], ss);  // squares are exact
-        ss = group_sum<16>(ss);
-        const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)kHeadDim), p.eps)));
-        float w[8], n[8];
-        unpack8<DT>(is_q ? qw : kw, w);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) n[e] = __fmul_rn(__fmul_rn(x[e], rstd), w[e]);
-        uint4 nv = pack8<DT>(n);
-
-        // partner half of each rotation pair
-        uint4 pv;
-        pv.x = __shfl_xor_sync(0xFFFFFFFFu, nv.x, 8);
-        pv.y = __shfl_xor_sync(0xFFFFFFFFu, nv.y, 8);
-        pv.z = __shfl_xor_sync(0xFFFFFFFFu, nv.z, 8);
-        pv.w = __shfl_xor_sync(0xFFFFFFFFu, nv.w, 8);
-        float m[8];
-        unpack8<DT>(nv, n);
-        unpack8<DT>(pv, m);
-
         const float c[8] = {__uint_as_float(c0.x), __uint_as_float(c0.y), __uint_as_float(c0.z),
                             __uint_as_float(c0.w), __uint_as_float(c1.x), __uint_as_float(c1.y),
                             __uint_as_float(c1.z), __uint_as_float(c1.w)};
         const float s[8] = {__uint_as_float(s0.x), __uint_as_float(s0.y), __uint_as_float(s0.z),
                             __uint_as_float(s0.w), __uint_as_float(s1.x), __uint_as_float(s1.y),
                             __uint_as_float(s1.z), __uint_as_float(s1.w)};
-        float o[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float a = __fmul_rn(n[e], c[e]);
-            const float b = __fmul_rn(m[e], s[e]);
-            o[e] = upper ? __fadd_rn(a, b) : __fsub_rn(a, b);
-        }
-        unpack8<DT>(pack8<DT>(o), o);  // FP8 from the dtype-rounded rotation
+        const uint8_t *qtok = static_cast<const uint8_t *>(p.q) + tok * p.q_stride * 2;
+        const uint8_t *ktok = static_cast<const uint8_t *>(p.k) + tok * p.k_stride * 2;
 
-        const float scale = is_q ? qscale : kscale;
-        float v[8];
+        for (int h0 = 0; h0 < heads; h0 += 2 * kPairs) {
+            uint4 xv[kPairs];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = __fdiv_rn(o[e], scale);
-        const uint2 code = e4m3x8(v);
-        if (ok) {
-            uint8_t *dst = is_q ? p.q_out + (tok * p.hq + h) * kHeadDim
-                                : p.k_out + (tok * p.hk + (h - p.hq)) * kHeadDim;
-            st8(dst + lane16 * 8, code.x, code.y);
+            for (int u = 0; u < kPairs; ++u) {
+                const int h = h0 + 2 * u + half;
+                const uint8_t *src = h < p.hq ? qtok + (int64_t)h * kHeadDim * 2
+                                              : ktok + (int64_t)(h - p.hq) * kHeadDim * 2;
+                xv[u] = h < heads ? ld_stream16(src + lane16 * 16) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < kPairs; ++u) {
+                const int h = h0 + 2 * u + half;
+                const bool is_q = h < p.hq;
+                // RMSNorm over the 16 lanes of the head row
+                float x[8];
+                unpack8<DT>(xv[u], x);
+                float ss = 0.0f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss = __fmaf_rn(x[e], x[e], ss);  // squares are exact
+                ss = group_sum<16>(ss);
+                const float rstd =
+                    __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)kHeadDim), p.eps)));
+                float w[8], n[8], m[8];
+                unpack8<DT>(is_q ? qw : kw, w);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) n[e] = __fmul_rn(__fmul_rn(x[e], rstd), w[e]);
+                const uint4 nv = pack8<DT>(n);
+                // the partner half of each rotation pair
+                uint4 pv;
+                pv.x = __shfl_xor_sync(0xFFFFFFFFu, nv.x, 8);
+                pv.y = __shfl_xor_sync(0xFFFFFFFFu, nv.y, 8);
+                pv.z = __shfl_xor_sync(0xFFFFFFFFu, nv.z, 8);
+                pv.w = __shfl_xor_sync(0xFFFFFFFFu, nv.w, 8);
+                unpack8<DT>(nv, n);
+                unpack8<DT>(pv, m);
+                float o[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float a = __fmul_rn(n[e], c[e]);
+                    const float b = __fmul_rn(m[e], s[e]);
+                    o[e] = upper ? __fadd_rn(a, b) : __fsub_rn(a, b);
+                }
+                unpack8<DT>(pack8<DT>(o), o);  // FP8 from the dtype-rounded rotation
+                const float scale = is_q ? qscale : kscale;
+                float v[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] = __fdiv_rn(o[e], scale);
+                const uint2 code = e4m3x8(v);
+                if (h < heads) {
+                    uint8_t *dst = is_q ? p.q_out + (tok * p.hq + h) * kHeadDim
+                                        : p.k_out + (tok * p.hk + (h - p.hq)) * kHeadDim;
+                    st8(dst + lane16 * 8, code.x, code.y);
+                }
+            }
         }
     }
 }
@@ -130,9 +135,7 @@ cudaError_t launch_qk_rmsnorm_rope_fp8(const QKParams &p, cudaStream_t stream)
             per_sm = 1;
         if (dev < 64) occ_cache[dev].store(per_sm, std::memory_order_relaxed);
     }
-    const int64_t nrows = p.n_tokens * (p.hq + p.hk);
-    const int64_t warps = (nrows + 1) / 2;
-    const int64_t need = (warps * 32 + kQKBlock - 1) / kQKBlock;
+    const int64_t need = (p.n_tokens * 32 + kQKBlock - 1) / kQKBlock;  // a warp per token
     const int64_t full = (int64_t)device_sms(dev) * per_sm;
     const int grid = (int)(need < full ? need : full);
     kern<<<grid, kQKBlock, 0, stream>>>(p);

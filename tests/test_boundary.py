@@ -77,11 +77,14 @@ def qk(L, **kw):
 @pytest.mark.parametrize("call", [fp8, nvfp4])
 def test_row_call_rejections(L, call):
     assert call(L, rows=0) == OK  # nothing to do, no launch
+    assert call(L, rows=0, x=None, r=None, ro=None, q=None) == OK  # empty tensors, null data
     assert call(L, x=None) == NULL
     assert call(L, w=None) == NULL
     assert call(L, s=None) == NULL
     assert call(L, q=None) == NULL
     assert call(L, rows=-1) == SHAPE
+    assert call(L, rows=0, hidden=136) == SHAPE
+    assert call(L, rows=0, dt=7) == DTYPE
     assert call(L, hidden=0) == SHAPE
     assert call(L, hidden=136) == SHAPE  # not a multiple of 16
     assert call(L, hidden=32768 + 16) == UNSUP
@@ -120,6 +123,7 @@ def test_amax_rejections(L):
 
 def test_qk_rejections(L):
     assert qk(L, T=0) == OK
+    assert qk(L, T=0, q=None, k=None, pos=None, cs=None) == OK
     assert qk(L, hd=64) == UNSUP
     assert qk(L, dt=5) == DTYPE
     assert qk(L, T=-1) == SHAPE
