@@ -174,6 +174,63 @@ __device__ __forceinline__ float e4m3_value(uint32_t byte)
     return f;
 }
 
+// ---------------------------------------------------------------- division
+// IEEE single operations, round to nearest even (PTX rcp.rn / div.rn are the
+// correctly rounded reciprocal and quotient).
+__device__ __forceinline__ float rcp_rn(float x)
+{
+    float r;
+    asm("rcp.rn.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ float div_rn(float a, float b)
+{
+    float r;
+    asm("div.rn.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float mul_rn(float a, float b)
+{
+    float r;
+    asm("mul.rn.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float fma_rn(float a, float b, float c)
+{
+    float r;
+    asm("fma.rn.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// a / b correctly rounded, for a divisor b shared by many dividends (the FP8
+// dequant scale, the constant 6 of the NVFP4 block scale).  Method: Markstein's
+// division theorem (P. Markstein, "Computation of elementary functions on the
+// IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with
+// y = RN(1/b) and q = RN(a * y), which is within one ulp of a/b, the remainder
+// r = a - b q is exact in one FMA and RN(q + r y) = RN(a/b), barring overflow
+// and underflow.  Guards: a zero dividend returns a * y (IEEE sign of the zero
+// quotient); |q| > 2^20 returns q (beyond 2^20 every consumer here saturates:
+// E4M3 at 448); divisors outside [2^-120, 2^120] fall back to __fdiv_rn.
+// Quotients in the fp32 subnormal range may differ from __fdiv_rn in the last
+// place; their E4M3 / E2M1 codes are the signed zero either way.
+struct DivBy {
+    float b, y;
+    bool fast;
+    __device__ __forceinline__ explicit DivBy(float b_) : b(b_), y(rcp_rn(b_))
+    {
+        const float m = fabsf(b_);
+        fast = m >= 0x1p-120f && m <= 0x1p120f;
+    }
+    __device__ __forceinline__ float operator()(float a) const
+    {
+        if (!fast) return div_rn(a, b);
+        const float q = mul_rn(a, y);
+        if (a == 0.0f || fabsf(q) > 0x1p20f) return q;
+        const float r = fma_rn(-q, b, a);
+        return fma_rn(r, y, q);
+    }
+};
+
 // ---------------------------------------------------------------- reductions
 // Sum over aligned groups of G lanes (G a power of two <= 32) of one warp;
 // every lane of the group receives the same result, summed in the same

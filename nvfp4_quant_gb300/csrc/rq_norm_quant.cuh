@@ -57,7 +57,9 @@ add_rmsnorm_quant_kernel(const NormQuantParams p)
         wv[j] = k < nvec ? ld_keep16(static_cast<const uint8_t *>(p.w) + (int64_t)k * 16)
                          : make_uint4(0, 0, 0, 0);
     }
-    const float scale = MODE == MODE_AMAX ? 0.0f : ld_f32(p.scale);
+    const float scale = MODE == MODE_AMAX ? 1.0f : ld_f32(p.scale);
+    const DivBy by_scale(scale);  // FP8: y / scale
+    const DivBy by_six(6.0f);     // NVFP4: (gs * amax) / 6
     const bool sf_words = (p.hidden % 64) == 0;  // 4 block scales per 32-bit store
     float amax_acc = 0.0f;
     int parity = 0;
@@ -135,7 +137,7 @@ add_rmsnorm_quant_kernel(const NormQuantParams p)
             if (MODE == MODE_FP8) {
                 float v[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = __fdiv_rn(y[e], scale);
+                for (int e = 0; e < 8; ++e) v[e] = by_scale(y[e]);
                 const uint2 c = e4m3x8(v);
                 if (ok) st8(p.q + row * H + (int64_t)k * 8, c.x, c.y);
             } else if (MODE == MODE_NVFP4) {
@@ -143,7 +145,7 @@ add_rmsnorm_quant_kernel(const NormQuantParams p)
 #pragma unroll
                 for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(y[e]));
                 const float a = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));  // 16-element block
-                const float t2 = __fdiv_rn(__fmul_rn(scale, a), 6.0f);
+                const float t2 = by_six(__fmul_rn(scale, a));
                 const uint32_t sfc = e4m3x2(t2, 0.0f) & 0xFFu;
                 const float sfv = e4m3_value(sfc);
                 const float enc = sfv == 0.0f ? 0.0f : __fdiv_rn(scale, sfv);

@@ -44,8 +44,8 @@ qk_rmsnorm_rope_fp8_kernel(const QKParams p)
                               : make_uint4(0, 0, 0, 0);
     const uint4 kw = p.hk > 0 ? ld_keep16(static_cast<const uint8_t *>(p.kw) + lane16 * 16)
                               : make_uint4(0, 0, 0, 0);
-    const float qscale = p.hq > 0 ? ld_f32(p.q_scale) : 1.0f;
-    const float kscale = p.hk > 0 ? ld_f32(p.k_scale) : 1.0f;
+    const DivBy by_q(p.hq > 0 ? ld_f32(p.q_scale) : 1.0f);
+    const DivBy by_k(p.hk > 0 ? ld_f32(p.k_scale) : 1.0f);
 
     for (int64_t tok = warp0; tok < p.n_tokens; tok += nwarps) {
         int pos = ld_s32(p.pos + tok);
@@ -82,8 +82,9 @@ qk_rmsnorm_rope_fp8_kernel(const QKParams p)
 #pragma unroll
                 for (int e = 0; e < 8; ++e) ss = __fmaf_rn(x[e], x[e], ss);  // squares are exact
                 ss = group_sum<16>(ss);
+                // ss / 128 is an exact power-of-two scaling, as the division would be
                 const float rstd =
-                    __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)kHeadDim), p.eps)));
+                    __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(ss, 1.0f / kHeadDim), p.eps)));
                 float w[8], n[8], m[8];
                 unpack8<DT>(is_q ? qw : kw, w);
 #pragma unroll
@@ -105,10 +106,10 @@ qk_rmsnorm_rope_fp8_kernel(const QKParams p)
                     o[e] = upper ? __fadd_rn(a, b) : __fsub_rn(a, b);
                 }
                 unpack8<DT>(pack8<DT>(o), o);  // FP8 from the dtype-rounded rotation
-                const float scale = is_q ? qscale : kscale;
+                const DivBy &by = is_q ? by_q : by_k;
                 float v[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = __fdiv_rn(o[e], scale);
+                for (int e = 0; e < 8; ++e) v[e] = by(o[e]);
                 const uint2 code = e4m3x8(v);
                 if (h < heads) {
                     uint8_t *dst = is_q ? p.q_out + (tok * p.hq + h) * kHeadDim
