@@ -202,32 +202,38 @@ __device__ __forceinline__ float fma_rn(float a, float b, float c)
     return r;
 }
 
-// a / b correctly rounded, for a divisor b shared by many dividends (the FP8
-// dequant scale, the constant 6 of the NVFP4 block scale).  Method: Markstein's
-// division theorem (P. Markstein, "Computation of elementary functions on the
-// IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with
+// a / b for a divisor b > 0 shared by many dividends (the FP8 dequant scale,
+// the constant 6 of the NVFP4 block scale).  Method: Markstein's division
+// theorem (P. Markstein, "Computation of elementary functions on the IBM
+// RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with
 // y = RN(1/b) and q = RN(a * y), which is within one ulp of a/b, the remainder
 // r = a - b q is exact in one FMA and RN(q + r y) = RN(a/b), barring overflow
-// and underflow.  Guards: a zero dividend returns a * y (IEEE sign of the zero
-// quotient); |q| > 2^20 returns q (beyond 2^20 every consumer here saturates:
-// E4M3 at 448); divisors outside [2^-120, 2^120] fall back to __fdiv_rn.
-// Quotients in the fp32 subnormal range may differ from __fdiv_rn in the last
-// place; their E4M3 / E2M1 codes are the signed zero either way.
+// and underflow.  Here it runs on |a| clamped to 2^20 b and the sign of a is
+// put back at the end, which makes it branch-free:
+//   * for quotients with magnitude in [2^-40, 2^20) the result is the correctly
+//     rounded a / b, bit for bit;
+//   * larger quotients come out as about 2^20, and quotients below 2^-40 are
+//     within one ulp; every consumer here gives those the same code as the true
+//     quotient (E4M3 saturates at 448 and rounds anything below 2^-10 to a
+//     signed zero);
+//   * signed zeros keep their sign, a NaN dividend gives NaN, an infinite one
+//     2^20 (E4M3: 448, as satfinite gives for infinity).
+// Divisors outside [2^-40, 2^40] (or not positive) use the IEEE division.
 struct DivBy {
-    float b, y;
+    float b, y, clamp;
     bool fast;
-    __device__ __forceinline__ explicit DivBy(float b_) : b(b_), y(rcp_rn(b_))
+    __device__ __forceinline__ explicit DivBy(float b_) : b(b_), y(rcp_rn(b_)), clamp(b_ * 0x1p20f)
     {
-        const float m = fabsf(b_);
-        fast = m >= 0x1p-120f && m <= 0x1p120f;
+        fast = b_ >= 0x1p-40f && b_ <= 0x1p40f;
     }
     __device__ __forceinline__ float operator()(float a) const
     {
         if (!fast) return div_rn(a, b);
-        const float q = mul_rn(a, y);
-        if (a == 0.0f || fabsf(q) > 0x1p20f) return q;
-        const float r = fma_rn(-q, b, a);
-        return fma_rn(r, y, q);
+        float m;
+        asm("{ .reg .f32 t; abs.f32 t, %1; min.NaN.f32 %0, t, %2; }" : "=f"(m) : "f"(a), "f"(clamp));
+        const float q = mul_rn(m, y);
+        const float r = fma_rn(-q, b, m);
+        return copysignf(fma_rn(r, y, q), a);
     }
 };
 

@@ -7,14 +7,16 @@
 // (SGLang PR 32975), review thread (norm + RoPE + uniform FP8 store as one
 // kernel epilogue).  The mapping below is ours.
 //
-// Mapping.  One warp per token (grid-stride over tokens).  A head row (128
+// Mapping.  A warp takes one unit of work: 2 * kPairs consecutive heads of one
+// token (grid-stride over units, token-major).  A head row (128
 // elements = 256 bytes) is owned by 16 lanes, 8 elements (one 16-byte vector)
 // per lane: lanes 0-15 take the even heads of the token, lanes 16-31 the odd
 // ones.  NeoX RoPE pairs element i with i + 64, i.e. lane l with lane l ^ 8,
 // and both lanes of a pair use the same frequencies 8 * (l & 7) .. + 7, so
-// each lane loads its 8 cos and 8 sin values once per token and keeps them in
-// registers for every head.  Heads are processed kPairs pairs at a time, which
-// keeps kPairs 16-byte loads per lane in flight.  The sum of squares is a
+// each lane loads its 8 cos and 8 sin values once per unit and keeps them in
+// registers for all its heads.  The kPairs head loads of a unit are issued
+// before any of them is used, so each lane has kPairs 16-byte loads in
+// flight; units of a few heads keep the tail of the grid short.  The sum of squares is a
 // 16-lane shuffle tree; the rounded normalised values are exchanged with one
 // 4-word shuffle.
 #include "rq_device.cuh"
@@ -24,12 +26,12 @@
 
 namespace rq {
 
-constexpr int kQKBlock = 256;
+constexpr int kQKBlock = 128;
 constexpr int kHeadDim = 128;
 constexpr int kPairs = 4;  // head pairs per step: 8 heads, 4 loads in flight per lane
 
 template <typename DT>
-__global__ void __launch_bounds__(kQKBlock, 2)
+__global__ void __launch_bounds__(kQKBlock, 6)
 qk_rmsnorm_rope_fp8_kernel(const QKParams p)
 {
     const int lane16 = threadIdx.x & 15;
@@ -47,7 +49,11 @@ qk_rmsnorm_rope_fp8_kernel(const QKParams p)
     const DivBy by_q(p.hq > 0 ? ld_f32(p.q_scale) : 1.0f);
     const DivBy by_k(p.hk > 0 ? ld_f32(p.k_scale) : 1.0f);
 
-    for (int64_t tok = warp0; tok < p.n_tokens; tok += nwarps) {
+    const int groups = (heads + 2 * kPairs - 1) / (2 * kPairs);  // units per token
+    const int64_t n_units = p.n_tokens * groups;
+    for (int64_t unit = warp0; unit < n_units; unit += nwarps) {
+        const int64_t tok = unit / groups;
+        const int h0 = (int)(unit - tok * groups) * 2 * kPairs;
         int pos = ld_s32(p.pos + tok);
         pos = pos < 0 ? 0 : (pos >= p.max_pos ? (int)(p.max_pos - 1) : pos);
         const uint8_t *cs = reinterpret_cast<const uint8_t *>(p.cos_sin + (int64_t)pos * kHeadDim);
@@ -56,13 +62,17 @@ qk_rmsnorm_rope_fp8_kernel(const QKParams p)
         const float c[8] = {__uint_as_float(c0.x), __uint_as_float(c0.y), __uint_as_float(c0.z),
                             __uint_as_float(c0.w), __uint_as_float(c1.x), __uint_as_float(c1.y),
                             __uint_as_float(c1.z), __uint_as_float(c1.w)};
-        const float s[8] = {__uint_as_float(s0.x), __uint_as_float(s0.y), __uint_as_float(s0.z),
-                            __uint_as_float(s0.w), __uint_as_float(s1.x), __uint_as_float(s1.y),
-                            __uint_as_float(s1.z), __uint_as_float(s1.w)};
+        // lanes holding elements 0..63 subtract m * sin, the others add it:
+        // fold that sign into the sine once per unit (RN(-x) = -RN(x))
+        const uint32_t neg = upper ? 0u : 0x80000000u;
+        const float s[8] = {__uint_as_float(s0.x ^ neg), __uint_as_float(s0.y ^ neg),
+                            __uint_as_float(s0.z ^ neg), __uint_as_float(s0.w ^ neg),
+                            __uint_as_float(s1.x ^ neg), __uint_as_float(s1.y ^ neg),
+                            __uint_as_float(s1.z ^ neg), __uint_as_float(s1.w ^ neg)};
         const uint8_t *qtok = static_cast<const uint8_t *>(p.q) + tok * p.q_stride * 2;
         const uint8_t *ktok = static_cast<const uint8_t *>(p.k) + tok * p.k_stride * 2;
 
-        for (int h0 = 0; h0 < heads; h0 += 2 * kPairs) {
+        {
             uint4 xv[kPairs];
 #pragma unroll
             for (int u = 0; u < kPairs; ++u) {
@@ -82,9 +92,11 @@ qk_rmsnorm_rope_fp8_kernel(const QKParams p)
 #pragma unroll
                 for (int e = 0; e < 8; ++e) ss = __fmaf_rn(x[e], x[e], ss);  // squares are exact
                 ss = group_sum<16>(ss);
-                // ss / 128 is an exact power-of-two scaling, as the division would be
+                // ss / 128 is an exact power-of-two scaling, as the division would
+                // be; 1 / sqrt(.) as the correctly rounded reciprocal of the
+                // correctly rounded root
                 const float rstd =
-                    __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(ss, 1.0f / kHeadDim), p.eps)));
+                    rcp_rn(__fsqrt_rn(__fadd_rn(__fmul_rn(ss, 1.0f / kHeadDim), p.eps)));
                 float w[8], n[8], m[8];
                 unpack8<DT>(is_q ? qw : kw, w);
 #pragma unroll
@@ -100,11 +112,7 @@ qk_rmsnorm_rope_fp8_kernel(const QKParams p)
                 unpack8<DT>(pv, m);
                 float o[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float a = __fmul_rn(n[e], c[e]);
-                    const float b = __fmul_rn(m[e], s[e]);
-                    o[e] = upper ? __fadd_rn(a, b) : __fsub_rn(a, b);
-                }
+                for (int e = 0; e < 8; ++e) o[e] = __fadd_rn(__fmul_rn(n[e], c[e]), __fmul_rn(m[e], s[e]));
                 unpack8<DT>(pack8<DT>(o), o);  // FP8 from the dtype-rounded rotation
                 const DivBy &by = is_q ? by_q : by_k;
                 float v[8];
@@ -136,7 +144,8 @@ cudaError_t launch_qk_rmsnorm_rope_fp8(const QKParams &p, cudaStream_t stream)
             per_sm = 1;
         if (dev < 64) occ_cache[dev].store(per_sm, std::memory_order_relaxed);
     }
-    const int64_t need = (p.n_tokens * 32 + kQKBlock - 1) / kQKBlock;  // a warp per token
+    const int groups = (p.hq + p.hk + 2 * kPairs - 1) / (2 * kPairs);
+    const int64_t need = (p.n_tokens * groups * 32 + kQKBlock - 1) / kQKBlock;  // a warp per unit
     const int64_t full = (int64_t)device_sms(dev) * per_sm;
     const int grid = (int)(need < full ? need : full);
     kern<<<grid, kQKBlock, 0, stream>>>(p);

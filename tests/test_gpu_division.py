@@ -1,9 +1,9 @@
 """The kernels divide by a per-tensor scale with one multiply by the rounded
 reciprocal and one FMA correction (Markstein's theorem) instead of a full
 division per element.  This test compares that division with CUDA's correctly
-rounded __fdiv_rn over every finite fp32 dividend: the quotients must agree
-bit for bit wherever the quotient is a normal number up to 2^20, and the
-E4M3 codes everywhere."""
+rounded __fdiv_rn over every fp32 dividend: the quotients must agree bit for
+bit wherever the quotient's magnitude is in [2^-40, 2^20), and the E4M3 codes
+everywhere (NaN and infinite dividends included)."""
 import os
 import subprocess
 
