@@ -218,24 +218,28 @@ __device__ __forceinline__ float fma_rn(float a, float b, float c)
 //     signed zero);
 //   * signed zeros keep their sign, a NaN dividend gives NaN, an infinite one
 //     2^20 (E4M3: 448, as satfinite gives for infinity).
-// Divisors outside [2^-40, 2^40] (or not positive) use the IEEE division.
-struct DivBy {
+// Divisors outside [2^-40, 2^40] (or not positive) must use the IEEE division:
+// kernels test Divisor::fast once and run a body instantiated with
+// kFast = false for them, so the per-element path has no branch.
+struct Divisor {
     float b, y, clamp;
     bool fast;
-    __device__ __forceinline__ explicit DivBy(float b_) : b(b_), y(rcp_rn(b_)), clamp(b_ * 0x1p20f)
+    __device__ __forceinline__ explicit Divisor(float b_) : b(b_), y(rcp_rn(b_)), clamp(b_ * 0x1p20f)
     {
         fast = b_ >= 0x1p-40f && b_ <= 0x1p40f;
     }
-    __device__ __forceinline__ float operator()(float a) const
-    {
-        if (!fast) return div_rn(a, b);
-        float m;
-        asm("{ .reg .f32 t; abs.f32 t, %1; min.NaN.f32 %0, t, %2; }" : "=f"(m) : "f"(a), "f"(clamp));
-        const float q = mul_rn(m, y);
-        const float r = fma_rn(-q, b, m);
-        return copysignf(fma_rn(r, y, q), a);
-    }
 };
+
+template <bool kFast>
+__device__ __forceinline__ float div_by(float a, const Divisor &d)
+{
+    if (!kFast) return div_rn(a, d.b);
+    float m;
+    asm("{ .reg .f32 t; abs.f32 t, %1; min.NaN.f32 %0, t, %2; }" : "=f"(m) : "f"(a), "f"(d.clamp));
+    const float q = mul_rn(m, d.y);
+    const float r = fma_rn(-q, d.b, m);
+    return copysignf(fma_rn(r, d.y, q), a);
+}
 
 // ---------------------------------------------------------------- reductions
 // Sum over aligned groups of G lanes (G a power of two <= 32) of one warp;

@@ -36,9 +36,11 @@ struct GroupShape {
     static constexpr int kWarpsPerGroup = G > 32 ? G / 32 : 1;
 };
 
-template <typename DT, int G, int VPT, int MODE>
-__global__ void __launch_bounds__(GroupShape<G>::kBlock)
-add_rmsnorm_quant_kernel(const NormQuantParams p)
+// kFast: the FP8 divisor is in the range of the branch-free division (the
+// kernel picks the body once; see Divisor).
+template <typename DT, int G, int VPT, int MODE, bool kFast>
+__device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
+                                                       float (*red)[GroupShape<G>::kWarps])
 {
     using S = GroupShape<G>;
     const int tid = threadIdx.x;
@@ -46,8 +48,6 @@ add_rmsnorm_quant_kernel(const NormQuantParams p)
     const int grp = tid / G;
     const int nvec = p.nvec;
     const int64_t H = p.hidden;
-
-    __shared__ float red[2][S::kWarps];
 
     // weight vectors of this thread, kept for every row it processes
     uint4 wv[VPT];
@@ -58,8 +58,8 @@ add_rmsnorm_quant_kernel(const NormQuantParams p)
                          : make_uint4(0, 0, 0, 0);
     }
     const float scale = MODE == MODE_AMAX ? 1.0f : ld_f32(p.scale);
-    const DivBy by_scale(scale);  // FP8: y / scale
-    const DivBy by_six(6.0f);     // NVFP4: (gs * amax) / 6
+    const Divisor by_scale(scale);  // FP8: y / scale
+    const Divisor by_six(6.0f);     // NVFP4: (gs * amax) / 6
     const bool sf_words = (p.hidden % 64) == 0;  // 4 block scales per 32-bit store
     float amax_acc = 0.0f;
     int parity = 0;
@@ -137,7 +137,7 @@ add_rmsnorm_quant_kernel(const NormQuantParams p)
             if (MODE == MODE_FP8) {
                 float v[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = by_scale(y[e]);
+                for (int e = 0; e < 8; ++e) v[e] = div_by<kFast>(y[e], by_scale);
                 const uint2 c = e4m3x8(v);
                 if (ok) st8(p.q + row * H + (int64_t)k * 8, c.x, c.y);
             } else if (MODE == MODE_NVFP4) {
@@ -145,7 +145,7 @@ add_rmsnorm_quant_kernel(const NormQuantParams p)
 #pragma unroll
                 for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(y[e]));
                 const float a = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));  // 16-element block
-                const float t2 = by_six(__fmul_rn(scale, a));
+                const float t2 = div_by<true>(__fmul_rn(scale, a), by_six);
                 const uint32_t sfc = e4m3x2(t2, 0.0f) & 0xFFu;
                 const float sfv = e4m3_value(sfc);
                 const float enc = sfv == 0.0f ? 0.0f : __fdiv_rn(scale, sfv);
@@ -186,6 +186,17 @@ add_rmsnorm_quant_kernel(const NormQuantParams p)
             atomicMax(reinterpret_cast<unsigned int *>(p.amax), __float_as_uint(r));
         }
     }
+}
+
+template <typename DT, int G, int VPT, int MODE>
+__global__ void __launch_bounds__(GroupShape<G>::kBlock)
+add_rmsnorm_quant_kernel(const NormQuantParams p)
+{
+    __shared__ float red[2][GroupShape<G>::kWarps];
+    if (MODE == MODE_FP8 && !Divisor(ld_f32(p.scale)).fast)
+        add_rmsnorm_quant_body<DT, G, VPT, MODE, false>(p, red);
+    else
+        add_rmsnorm_quant_body<DT, G, VPT, MODE, true>(p, red);
 }
 
 }  // namespace rq

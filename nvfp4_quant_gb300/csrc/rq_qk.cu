@@ -30,9 +30,8 @@ constexpr int kQKBlock = 128;
 constexpr int kHeadDim = 128;
 constexpr int kPairs = 4;  // head pairs per step: 8 heads, 4 loads in flight per lane
 
-template <typename DT>
-__global__ void __launch_bounds__(kQKBlock, 6)
-qk_rmsnorm_rope_fp8_kernel(const QKParams p)
+template <typename DT, bool kFast>
+__device__ __forceinline__ void qk_body(const QKParams &p)
 {
     const int lane16 = threadIdx.x & 15;
     const int half = (threadIdx.x >> 4) & 1;            // even or odd heads
@@ -46,8 +45,8 @@ qk_rmsnorm_rope_fp8_kernel(const QKParams p)
                               : make_uint4(0, 0, 0, 0);
     const uint4 kw = p.hk > 0 ? ld_keep16(static_cast<const uint8_t *>(p.kw) + lane16 * 16)
                               : make_uint4(0, 0, 0, 0);
-    const DivBy by_q(p.hq > 0 ? ld_f32(p.q_scale) : 1.0f);
-    const DivBy by_k(p.hk > 0 ? ld_f32(p.k_scale) : 1.0f);
+    const Divisor by_q(p.hq > 0 ? ld_f32(p.q_scale) : 1.0f);
+    const Divisor by_k(p.hk > 0 ? ld_f32(p.k_scale) : 1.0f);
 
     const int groups = (heads + 2 * kPairs - 1) / (2 * kPairs);  // units per token
     const int64_t n_units = p.n_tokens * groups;
@@ -114,10 +113,10 @@ qk_rmsnorm_rope_fp8_kernel(const QKParams p)
 #pragma unroll
                 for (int e = 0; e < 8; ++e) o[e] = __fadd_rn(__fmul_rn(n[e], c[e]), __fmul_rn(m[e], s[e]));
                 unpack8<DT>(pack8<DT>(o), o);  // FP8 from the dtype-rounded rotation
-                const DivBy &by = is_q ? by_q : by_k;
+                const Divisor &by = is_q ? by_q : by_k;
                 float v[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = by(o[e]);
+                for (int e = 0; e < 8; ++e) v[e] = div_by<kFast>(o[e], by);
                 const uint2 code = e4m3x8(v);
                 if (h < heads) {
                     uint8_t *dst = is_q ? p.q_out + (tok * p.hq + h) * kHeadDim
@@ -127,6 +126,18 @@ qk_rmsnorm_rope_fp8_kernel(const QKParams p)
             }
         }
     }
+}
+
+template <typename DT>
+__global__ void __launch_bounds__(kQKBlock, 6)
+qk_rmsnorm_rope_fp8_kernel(const QKParams p)
+{
+    const bool fast = (p.hq == 0 || Divisor(ld_f32(p.q_scale)).fast) &&
+                      (p.hk == 0 || Divisor(ld_f32(p.k_scale)).fast);
+    if (fast)
+        qk_body<DT, true>(p);
+    else
+        qk_body<DT, false>(p);
 }
 
 template <typename DT>

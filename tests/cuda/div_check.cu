@@ -1,4 +1,4 @@
-// div_check.cu -- compares the library's shared-divisor division (rq::DivBy,
+// div_check.cu -- compares the library's shared-divisor division (rq::div_by,
 // Markstein's correction step) with CUDA's correctly rounded __fdiv_rn over
 // every finite fp32 dividend, for each divisor given on the command line.
 // Prints, per divisor: the fp32 quotients that differ where the reference
@@ -15,14 +15,14 @@ __device__ unsigned int g_first_bad;
 
 __global__ void check(float b)
 {
-    const rq::DivBy by(b);
+    const rq::Divisor d(b);
     const unsigned long long n = 1ull << 32;
     for (unsigned long long i = blockIdx.x * (unsigned long long)blockDim.x + threadIdx.x; i < n;
          i += (unsigned long long)gridDim.x * blockDim.x) {
         const unsigned int bits = (unsigned int)i;
         const float a = __uint_as_float(bits);
         const float ref = __fdiv_rn(a, b);
-        const float got = by(a);
+        const float got = d.fast ? rq::div_by<true>(a, d) : rq::div_by<false>(a, d);
         const float m = fabsf(ref);
         if (m >= 0x1p-40f && m < 0x1p20f && __float_as_uint(ref) != __float_as_uint(got)) {
             if (atomicAdd(&g_quot_diff, 1ull) == 0) g_first_bad = bits;
