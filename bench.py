@@ -277,6 +277,7 @@ def run_ours(args):
 
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(args, wl, ws)
+    next_rows = measure_next_rows(wl, peak_kind_gbs=peaks()[0])
 
     peak, peak_kind = peaks()
     kernels = {}
@@ -322,6 +323,7 @@ def run_ours(args):
                      "frac_of_nominal_8tbs": round(dgbs / NOMINAL_HBM_GBS, 4),
                      "traffic": traffic, "alg_bytes": dbytes},
         "e2e": e2e,
+        "next_rows": next_rows,
         "gpu_launches": len(calls) * args.steps,
         "clocks": clk.summary(),
     }
@@ -332,6 +334,49 @@ def run_ours(args):
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def measure_next_rows(wl, peak_kind_gbs, iters=50):
+    """Dynamic-scale calls (timed on their own, outside the step): per-token
+    FP8 on the prefill workload and per-tensor dynamic FP8 / NVFP4 (amax pass +
+    fused pass) on the prefill / large NVFP4 workloads."""
+    rq, d = wl.rq, wl.d
+    f = lambda: torch.zeros(1, dtype=torch.float32, device="cuda")
+    row_scales = torch.empty(FP8_ROWS, dtype=torch.float32, device="cuda")
+    s3, g5 = f(), f()
+    cases = [
+        ("add_rmsnorm_fp8_per_token", FP8_ROWS,
+         FP8_ROWS * FP8_H * 7 + FP8_ROWS * 4 + FP8_H * 2,
+         lambda: rq.rq_add_rmsnorm_fp8_per_token(d["x3"], d["r3"], wl.ro3, wl.w3, EPS, wl.q3,
+                                                 row_scales)),
+        ("add_rmsnorm_fp8_dynamic", FP8_ROWS,
+         FP8_ROWS * FP8_H * (4 + 7) + 2 * FP8_H * 2 + 8,
+         lambda: rq.rq_add_rmsnorm_fp8_dynamic(d["x3"], d["r3"], wl.ro3, wl.w3, EPS, s3, wl.q3)),
+        ("add_rmsnorm_nvfp4_dynamic", NV_ROWS,
+         alg_bytes_nvfp4(NV_ROWS, NV_H) + NV_ROWS * NV_H * 4 + NV_H * 2 + 4,
+         lambda: rq.rq_add_rmsnorm_nvfp4_dynamic(d["x5"], d["r5"], wl.ro5, wl.w5, EPS, g5, wl.p5,
+                                                 wl.sf5, wl.y5)),
+    ]
+    out = {}
+    stream = torch.cuda.current_stream()
+    for name, rows, nbytes, fn in cases:
+        for _ in range(3):
+            fn()
+            wl.nvfp4() if rows == FP8_ROWS else wl.fp8()  # evict this call's inputs from L2
+        evs = []
+        for _ in range(iters):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            evs.append((a, b))
+            wl.nvfp4() if rows == FP8_ROWS else wl.fp8()
+        torch.cuda.synchronize()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out[name] = {"ms": round(ms, 5), "rows_per_s": rows / (ms / 1e3), "alg_bytes": nbytes,
+                     "gbs": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak_kind_gbs, 4)}
+    return out
 
 
 def run_e2e(args, wl, ws):

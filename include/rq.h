@@ -160,11 +160,53 @@ rq_status rq_add_rmsnorm_amax(const void *x, const void *residual_in,
                               rq_stream_t stream);
 
 /* d_scale = amax / 448 (the FP8 dequant scale) and d_gs = 448 * 6 / amax
- * (the NVFP4 global scale), each one fp32 division on the device. */
+ * (the NVFP4 global scale), each one fp32 division on the device (the plain
+ * formulas: a zero amax gives 0 and inf). */
 rq_status rq_fp8_scale_from_amax(const float *d_amax, float *d_scale,
                                  rq_stream_t stream);
 rq_status rq_nvfp4_global_scale_from_amax(const float *d_amax, float *d_gs,
                                           rq_stream_t stream);
+
+/*
+ * Dynamic scales (residual add + RMSNorm, then the quantiser with a scale
+ * taken from the norm output itself).
+ * Source: the pages' per-tensor scales are absolute maxima of the tensor
+ * ("Add AutoDeploy NVFP4 RMSNorm quant fusion", Changes: reference module
+ * with input-scale calibration); "Add NanoJet backend for AutoDeploy
+ * prefill-only FP8 inference", Description: FP8 quantisation in the norm
+ * epilogue.  A maximum of zero (all-zero row or tensor) gives the scale 1,
+ * so that the codes are zeros rather than the 0/0 of the plain formula.
+ *
+ * rq_add_rmsnorm_fp8_per_token: one pass; row r gets the dequant scale
+ *   d_row_scales[r] = amax_r(|y|) / 448 (fp32, written) and
+ *   q = E4M3(y / d_row_scales[r]).  d_row_scales: [rows] fp32.
+ * rq_add_rmsnorm_fp8_dynamic / rq_add_rmsnorm_nvfp4_dynamic: two passes over
+ *   x and residual (the first finds the tensor's amax, the second is the
+ *   fused call); *d_scale_out receives the scale used (FP8: amax / 448;
+ *   NVFP4: 2688 / amax).  The first pass accumulates the maximum in
+ *   *d_scale_out itself, so no workspace is needed.  In-place residual is
+ *   allowed (the first pass only reads).
+ * Other arguments as in rq_add_rmsnorm_fp8 / rq_add_rmsnorm_nvfp4.
+ */
+rq_status rq_add_rmsnorm_fp8_per_token(const void *x, const void *residual_in,
+                                       void *residual_out, const void *weight,
+                                       float eps, uint8_t *q_out,
+                                       float *d_row_scales, void *norm_out,
+                                       int64_t rows, int64_t hidden,
+                                       rq_dtype dt, rq_stream_t stream);
+rq_status rq_add_rmsnorm_fp8_dynamic(const void *x, const void *residual_in,
+                                     void *residual_out, const void *weight,
+                                     float eps, float *d_scale_out,
+                                     uint8_t *q_out, void *norm_out,
+                                     int64_t rows, int64_t hidden, rq_dtype dt,
+                                     rq_stream_t stream);
+rq_status rq_add_rmsnorm_nvfp4_dynamic(const void *x, const void *residual_in,
+                                       void *residual_out, const void *weight,
+                                       float eps, float *d_global_scale_out,
+                                       uint8_t *q_packed, uint8_t *block_scales,
+                                       void *norm_out, int64_t rows,
+                                       int64_t hidden, rq_dtype dt,
+                                       rq_stream_t stream);
 
 /* Output sizes of the NVFP4 call (the linear, unswizzled layout):
  * rows * hidden / 2 packed bytes and rows * hidden / 16 scale bytes.

@@ -31,6 +31,12 @@ SIGNATURES = {
     "rq_qk_rmsnorm_rope_fp8": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp, _vp,
                                       _f32, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _int, _vp]),
     "rq_add_rmsnorm_amax": (_int, [_vp, _vp, _vp, _f32, _vp, _i64, _i64, _int, _vp]),
+    "rq_add_rmsnorm_fp8_per_token": (_int, [_vp, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _i64, _i64,
+                                            _int, _vp]),
+    "rq_add_rmsnorm_fp8_dynamic": (_int, [_vp, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _i64, _i64,
+                                          _int, _vp]),
+    "rq_add_rmsnorm_nvfp4_dynamic": (_int, [_vp, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _i64,
+                                            _i64, _int, _vp]),
     "rq_fp8_scale_from_amax": (_int, [_vp, _vp, _vp]),
     "rq_nvfp4_global_scale_from_amax": (_int, [_vp, _vp, _vp]),
     "rq_nvfp4_packed_bytes": (ctypes.c_size_t, [_i64, _i64]),
@@ -131,6 +137,38 @@ def rq_add_rmsnorm_amax(x, residual_in, weight, eps, amax_out, stream=None):
     rows, hidden = _rows(x, residual_in)
     _check(lib().rq_add_rmsnorm_amax(_ptr(x), _ptr(residual_in), _ptr(weight), float(eps),
                                      _ptr(amax_out), rows, hidden, _dt(x), _stream(stream)))
+
+
+def rq_add_rmsnorm_fp8_per_token(x, residual_in, residual_out, weight, eps, q_out, row_scales,
+                                 norm_out=None, stream=None):
+    """Residual add + RMSNorm + FP8 with per-row dynamic scales (include/rq.h).
+    row_scales: float32 [rows], written."""
+    rows, hidden = _rows(x, residual_in, residual_out, norm_out)
+    _check(lib().rq_add_rmsnorm_fp8_per_token(_ptr(x), _ptr(residual_in), _ptr(residual_out),
+                                              _ptr(weight), float(eps), _ptr(q_out),
+                                              _ptr(row_scales), _ptr(norm_out), rows, hidden,
+                                              _dt(x), _stream(stream)))
+
+
+def rq_add_rmsnorm_fp8_dynamic(x, residual_in, residual_out, weight, eps, scale_out, q_out,
+                               norm_out=None, stream=None):
+    """Residual add + RMSNorm + FP8 with the per-tensor scale amax/448 computed
+    on the device (include/rq.h); scale_out: 1-element float32, written."""
+    rows, hidden = _rows(x, residual_in, residual_out, norm_out)
+    _check(lib().rq_add_rmsnorm_fp8_dynamic(_ptr(x), _ptr(residual_in), _ptr(residual_out),
+                                            _ptr(weight), float(eps), _ptr(scale_out), _ptr(q_out),
+                                            _ptr(norm_out), rows, hidden, _dt(x), _stream(stream)))
+
+
+def rq_add_rmsnorm_nvfp4_dynamic(x, residual_in, residual_out, weight, eps, global_scale_out,
+                                 q_packed, block_scales, norm_out=None, stream=None):
+    """Residual add + RMSNorm + NVFP4 with the global scale 2688/amax computed
+    on the device (include/rq.h); global_scale_out: 1-element float32, written."""
+    rows, hidden = _rows(x, residual_in, residual_out, norm_out)
+    _check(lib().rq_add_rmsnorm_nvfp4_dynamic(_ptr(x), _ptr(residual_in), _ptr(residual_out),
+                                              _ptr(weight), float(eps), _ptr(global_scale_out),
+                                              _ptr(q_packed), _ptr(block_scales), _ptr(norm_out),
+                                              rows, hidden, _dt(x), _stream(stream)))
 
 
 def rq_fp8_scale_from_amax(amax, scale_out, stream=None):

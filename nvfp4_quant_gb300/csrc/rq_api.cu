@@ -79,6 +79,7 @@ rq::NormQuantParams make_params(const void *x, const void *res_in, void *res_out
     p.sf = sf;
     p.scale = scale;
     p.amax = amax;
+    p.row_scales = nullptr;
     p.eps = eps;
     p.rows = rows;
     p.hidden = (int)hidden;
@@ -107,6 +108,53 @@ int device_sms(int dev)
     return v;
 }
 }  // namespace rq
+
+namespace {
+
+// Dynamic per-tensor scale: the amax pass accumulates straight into the
+// caller's scale output, which is then turned into the scale in place and read
+// by the fused pass -- no workspace.
+template <int MODE>
+rq_status dynamic_tensor_call(const void *x, const void *residual_in, void *residual_out,
+                                     const void *weight, float eps, float *d_scale_out, uint8_t *q,
+                                     uint8_t *sf, void *norm_out, int64_t rows, int64_t hidden,
+                                     rq_dtype dt, rq_stream_t stream)
+{
+    rq_status st = check_rows(rows, hidden, dt);
+    if (st != RQ_OK) return st;
+    if (!d_scale_out) return RQ_ERR_NULL;
+    if (!aligned4(d_scale_out)) return RQ_ERR_MISALIGNED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int nvfp4 = MODE == rq::MODE_NVFP4;
+    if (rows > 0) {
+        if (!x || !residual_in || !residual_out || !weight || !q || (nvfp4 && !sf)) return RQ_ERR_NULL;
+        if (!aligned16(x) || !aligned16(residual_in) || !aligned16(residual_out) ||
+            !aligned16(weight) || !aligned16(q) || (nvfp4 && !aligned16(sf)) ||
+            (norm_out && !aligned16(norm_out)))
+            return RQ_ERR_MISALIGNED;
+        const int64_t tb = rows * hidden * 2;
+        const Span ins[] = {span(x, tb), span(residual_in, tb), span(weight, hidden * 2)};
+        const Span outs[] = {span(residual_out, tb), span(norm_out, tb),
+                             span(q, nvfp4 ? rows * hidden / 2 : rows * hidden),
+                             span(nvfp4 ? sf : nullptr, rows * hidden / 16), span(d_scale_out, 4)};
+        if (bad_alias(outs, 5, ins, 3, 0, 1)) return RQ_ERR_ALIAS;
+    }
+    st = cuda_status(cudaMemsetAsync(d_scale_out, 0, sizeof(float), s));
+    if (st != RQ_OK) return st;
+    if (rows > 0) {
+        auto pa = make_params(x, residual_in, nullptr, weight, eps, nullptr, nullptr, nullptr, nullptr,
+                              d_scale_out, rows, hidden);
+        st = launch_rows<rq::MODE_AMAX>(pa, dt, stream);
+        if (st != RQ_OK) return st;
+    }
+    st = cuda_status(rq::launch_scale_from_amax(d_scale_out, d_scale_out, nvfp4, 1, s));
+    if (st != RQ_OK || rows == 0) return st;
+    auto p = make_params(x, residual_in, residual_out, weight, eps, d_scale_out, q, sf, norm_out,
+                         nullptr, rows, hidden);
+    return launch_rows<MODE>(p, dt, stream);
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -183,7 +231,7 @@ static rq_status scale_from_amax(const float *d_amax, float *d_out, int nvfp4, r
     if (!d_amax || !d_out) return RQ_ERR_NULL;
     if (!aligned4(d_amax) || !aligned4(d_out)) return RQ_ERR_MISALIGNED;
     return cuda_status(
-        rq::launch_scale_from_amax(d_amax, d_out, nvfp4, reinterpret_cast<cudaStream_t>(stream)));
+        rq::launch_scale_from_amax(d_amax, d_out, nvfp4, 0, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 rq_status rq_fp8_scale_from_amax(const float *d_amax, float *d_scale, rq_stream_t stream)
@@ -194,6 +242,48 @@ rq_status rq_fp8_scale_from_amax(const float *d_amax, float *d_scale, rq_stream_
 rq_status rq_nvfp4_global_scale_from_amax(const float *d_amax, float *d_gs, rq_stream_t stream)
 {
     return scale_from_amax(d_amax, d_gs, 1, stream);
+}
+
+rq_status rq_add_rmsnorm_fp8_per_token(const void *x, const void *residual_in, void *residual_out,
+                                       const void *weight, float eps, uint8_t *q_out,
+                                       float *d_row_scales, void *norm_out, int64_t rows,
+                                       int64_t hidden, rq_dtype dt, rq_stream_t stream)
+{
+    rq_status st = check_rows(rows, hidden, dt);
+    if (st != RQ_OK || rows == 0) return st;
+    if (!x || !residual_in || !residual_out || !weight || !q_out || !d_row_scales) return RQ_ERR_NULL;
+    if (!aligned16(x) || !aligned16(residual_in) || !aligned16(residual_out) || !aligned16(weight) ||
+        !aligned16(q_out) || (norm_out && !aligned16(norm_out)) || !aligned4(d_row_scales))
+        return RQ_ERR_MISALIGNED;
+    const int64_t tb = rows * hidden * 2;
+    const Span ins[] = {span(x, tb), span(residual_in, tb), span(weight, hidden * 2)};
+    const Span outs[] = {span(residual_out, tb), span(norm_out, tb), span(q_out, rows * hidden),
+                         span(d_row_scales, rows * 4)};
+    if (bad_alias(outs, 4, ins, 3, 0, 1)) return RQ_ERR_ALIAS;
+    auto p = make_params(x, residual_in, residual_out, weight, eps, nullptr, q_out, nullptr, norm_out,
+                         nullptr, rows, hidden);
+    p.row_scales = d_row_scales;
+    return launch_rows<rq::MODE_FP8_ROW>(p, dt, stream);
+}
+
+rq_status rq_add_rmsnorm_fp8_dynamic(const void *x, const void *residual_in, void *residual_out,
+                                     const void *weight, float eps, float *d_scale_out,
+                                     uint8_t *q_out, void *norm_out, int64_t rows, int64_t hidden,
+                                     rq_dtype dt, rq_stream_t stream)
+{
+    return dynamic_tensor_call<rq::MODE_FP8>(x, residual_in, residual_out, weight, eps, d_scale_out,
+                                             q_out, nullptr, norm_out, rows, hidden, dt, stream);
+}
+
+rq_status rq_add_rmsnorm_nvfp4_dynamic(const void *x, const void *residual_in, void *residual_out,
+                                       const void *weight, float eps, float *d_global_scale_out,
+                                       uint8_t *q_packed, uint8_t *block_scales, void *norm_out,
+                                       int64_t rows, int64_t hidden, rq_dtype dt,
+                                       rq_stream_t stream)
+{
+    return dynamic_tensor_call<rq::MODE_NVFP4>(x, residual_in, residual_out, weight, eps,
+                                               d_global_scale_out, q_packed, block_scales, norm_out,
+                                               rows, hidden, dt, stream);
 }
 
 rq_status rq_qk_rmsnorm_rope_fp8(const void *q, const void *k, int64_t q_token_stride,

@@ -20,6 +20,7 @@ struct NormQuantParams {
     uint8_t *sf;         // NVFP4 block scales [rows, H/16]
     const float *scale;  // FP8 dequant scale or NVFP4 global scale
     float *amax;         // amax-mode output
+    float *row_scales;   // per-row FP8 scales [rows] (per-token mode)
     float eps;
     int64_t rows;
     int hidden;
@@ -45,7 +46,7 @@ struct QKParams {
     uint8_t *k_out;
 };
 
-enum QuantMode { MODE_FP8 = 0, MODE_NVFP4 = 1, MODE_AMAX = 2 };
+enum QuantMode { MODE_FP8 = 0, MODE_NVFP4 = 1, MODE_AMAX = 2, MODE_FP8_ROW = 3 };
 
 // SM count of device `dev` (cached).
 int device_sms(int dev);
@@ -56,6 +57,9 @@ cudaError_t launch_add_rmsnorm(const NormQuantParams &p, cudaStream_t stream);
 template <typename DT>
 cudaError_t launch_qk_rmsnorm_rope_fp8(const QKParams &p, cudaStream_t stream);
 
-cudaError_t launch_scale_from_amax(const float *amax, float *out, int nvfp4, cudaStream_t stream);
+// out = amax / 448 (nvfp4 == 0) or 2688 / amax (nvfp4 == 1); with
+// zero_to_one, a zero amax gives 1.  out may equal amax.
+cudaError_t launch_scale_from_amax(const float *amax, float *out, int nvfp4, int zero_to_one,
+                                   cudaStream_t stream);
 
 }  // namespace rq

@@ -57,7 +57,7 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
         wv[j] = k < nvec ? ld_keep16(static_cast<const uint8_t *>(p.w) + (int64_t)k * 16)
                          : make_uint4(0, 0, 0, 0);
     }
-    const float scale = MODE == MODE_AMAX ? 1.0f : ld_f32(p.scale);
+    const float scale = (MODE == MODE_FP8 || MODE == MODE_NVFP4) ? ld_f32(p.scale) : 1.0f;
     const Divisor by_scale(scale);  // FP8: y / scale
     const Divisor by_six(6.0f);     // NVFP4: (gs * amax) / 6
     const bool sf_words = (p.hidden % 64) == 0;  // 4 block scales per 32-bit store
@@ -120,6 +120,7 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
         const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, p.eps)));
 
         // ---- normalise, store, quantise
+        float row_amax = 0.0f;  // per-token mode: max |y| of this thread's part of the row
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
             const int k = j * G + t;
@@ -164,11 +165,52 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
                 } else if (ok && (k & 1) == 0) {
                     st1(sfrow + k / 2, sfc);
                 }
+            } else if (MODE == MODE_FP8_ROW) {
+                sv[j] = yv;  // residual' is stored; keep the rounded y for the second pass
+                if (ok) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) row_amax = fmaxf(row_amax, fabsf(y[e]));
+                }
             } else {  // MODE_AMAX
                 if (ok) {
 #pragma unroll
                     for (int e = 0; e < 8; ++e) amax_acc = fmaxf(amax_acc, fabsf(y[e]));
                 }
+            }
+        }
+
+        if (MODE == MODE_FP8_ROW) {
+            // the row's absolute maximum, its scale amax / 448 (1 for a zero
+            // row), then the codes from the rounded y kept in registers
+            if (G <= 32) {
+                row_amax = group_max<(G <= 32 ? G : 32)>(row_amax);
+            } else {
+                row_amax = group_max<32>(row_amax);
+                if ((tid & 31) == 0) red[parity][tid >> 5] = row_amax;
+                __syncthreads();
+                const int w0 = grp * S::kWarpsPerGroup;
+                row_amax = 0.0f;
+#pragma unroll
+                for (int i = 0; i < S::kWarpsPerGroup; ++i) row_amax = fmaxf(row_amax, red[parity][w0 + i]);
+                parity ^= 1;
+            }
+            const float rs = row_amax > 0.0f ? div_rn(row_amax, 448.0f) : 1.0f;
+            const Divisor d(rs);
+            if (row_ok && t == 0) p.row_scales[row] = rs;
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const int k = j * G + t;
+                float y[8], v[8];
+                unpack8<DT>(sv[j], y);
+                if (d.fast) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] = div_by<true>(y[e], d);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] = div_by<false>(y[e], d);
+                }
+                const uint2 c = e4m3x8(v);
+                if (row_ok && k < nvec) st8(p.q + row * H + (int64_t)k * 8, c.x, c.y);
             }
         }
     }

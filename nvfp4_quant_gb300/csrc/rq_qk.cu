@@ -167,15 +167,16 @@ template cudaError_t launch_qk_rmsnorm_rope_fp8<BF16>(const QKParams &, cudaStre
 template cudaError_t launch_qk_rmsnorm_rope_fp8<FP16>(const QKParams &, cudaStream_t);
 
 // ---- scales from a calibrated amax: one fp32 IEEE division each
-__global__ void scale_from_amax_kernel(const float *amax, float *out, int nvfp4)
+__global__ void scale_from_amax_kernel(const float *amax, float *out, int nvfp4, int zero_to_one)
 {
-    const float a = ld_f32(amax);
-    *out = nvfp4 ? __fdiv_rn(2688.0f, a) : __fdiv_rn(a, 448.0f);
+    const float a = *amax;  // plain load: out may alias amax
+    *out = (zero_to_one && !(a > 0.0f)) ? 1.0f : nvfp4 ? __fdiv_rn(2688.0f, a) : __fdiv_rn(a, 448.0f);
 }
 
-cudaError_t launch_scale_from_amax(const float *amax, float *out, int nvfp4, cudaStream_t stream)
+cudaError_t launch_scale_from_amax(const float *amax, float *out, int nvfp4, int zero_to_one,
+                                   cudaStream_t stream)
 {
-    scale_from_amax_kernel<<<1, 1, 0, stream>>>(amax, out, nvfp4);
+    scale_from_amax_kernel<<<1, 1, 0, stream>>>(amax, out, nvfp4, zero_to_one);
     return cudaGetLastError();
 }
 

@@ -51,6 +51,9 @@ def lib():
                                                 u16p, u16p, u8p, u8p]),
             "oracle_amax": (ctypes.c_float, [i32, u16p, i64]),
             "oracle_fp8_scale_from_amax": (ctypes.c_float, [f32]),
+            "oracle_fp8_dynamic_scale": (ctypes.c_float, [f32]),
+            "oracle_nvfp4_dynamic_gs": (ctypes.c_float, [f32]),
+            "oracle_quant_fp8_per_row": (None, [i32, u16p, i64, i64, u8p, fp]),
             "oracle_nvfp4_gs_from_amax": (ctypes.c_float, [f32]),
             "oracle_qk_rmsnorm_rope": (None, [i32, u16p, i64, i64, i32, i32, u16p, f32, i32p,
                                               fp, i64, u16p]),
@@ -185,6 +188,25 @@ def fp8_scale_from_amax(a):
 
 def nvfp4_gs_from_amax(a):
     return float(lib().oracle_nvfp4_gs_from_amax(a))
+
+
+def fp8_dynamic_scale(a):
+    return float(lib().oracle_fp8_dynamic_scale(a))
+
+
+def nvfp4_dynamic_gs(a):
+    return float(lib().oracle_nvfp4_dynamic_gs(a))
+
+
+def quant_fp8_per_row(dt, y):
+    """(codes, per-row scales) of the per-token dynamic FP8 quantiser."""
+    y = _u16(y)
+    rows, hidden = y.shape
+    q = np.empty(y.shape, np.uint8)
+    sc = np.empty(rows, np.float32)
+    lib().oracle_quant_fp8_per_row(_DT[dt], _p(y, ctypes.c_uint16), rows, hidden,
+                                   _p(q, ctypes.c_uint8), _p(sc, ctypes.c_float))
+    return q, sc
 
 
 def qk_rmsnorm_rope(dt, src, token_stride, n_tokens, n_heads, head_dim, w, eps,

@@ -281,6 +281,27 @@ float oracle_amax(int dt, const uint16_t *v, int64_t n)
 float oracle_fp8_scale_from_amax(float amax) { float s = amax / 448.0f; return s; }
 float oracle_nvfp4_gs_from_amax(float amax) { float g = 2688.0f / amax; return g; }
 
+/* ---- dynamic scales (the plain formulas, with 1 for a zero maximum) ---- */
+float oracle_fp8_dynamic_scale(float amax)
+{
+    return amax > 0.0f ? oracle_fp8_scale_from_amax(amax) : 1.0f;
+}
+
+float oracle_nvfp4_dynamic_gs(float amax)
+{
+    return amax > 0.0f ? oracle_nvfp4_gs_from_amax(amax) : 1.0f;
+}
+
+void oracle_quant_fp8_per_row(int dt, const uint16_t *y, int64_t rows,
+                              int64_t hidden, uint8_t *q, float *row_scales)
+{
+    for (int64_t row = 0; row < rows; ++row) {
+        float scale = oracle_fp8_dynamic_scale(oracle_amax(dt, y + row * hidden, hidden));
+        row_scales[row] = scale;
+        oracle_quant_fp8(dt, y + row * hidden, hidden, scale, q + row * hidden);
+    }
+}
+
 /* ---- Q/K RMSNorm + NeoX RoPE ([P1] fused Q/K RMSNorm and RoPE,
  *      [P3] norm + RoPE + uniform FP8 store) ---- */
 void oracle_qk_rmsnorm_rope(int dt, const uint16_t *src, int64_t token_stride,

@@ -97,6 +97,17 @@ void oracle_add_rmsnorm_nvfp4(int dt, const uint16_t *x, const uint16_t *r,
                               int64_t rows, int64_t hidden, uint16_t *s_out,
                               uint16_t *y_out, uint8_t *packed, uint8_t *sf);
 
+/* Dynamic scales.  A scale derived from an absolute maximum of zero (an
+ * all-zero row or tensor) is taken as 1, so that every code is a signed zero
+ * and the dequantised values are zero, instead of the 0/0 of the plain
+ * formula.
+ *   per row:    scale_r = f32(amax_r / 448), q = E4M3sat(f32(y / scale_r))
+ *   per tensor: scale = f32(amax / 448) (FP8), gs = f32(2688 / amax) (NVFP4) */
+void oracle_quant_fp8_per_row(int dt, const uint16_t *y, int64_t rows,
+                              int64_t hidden, uint8_t *q, float *row_scales);
+float oracle_fp8_dynamic_scale(float amax);
+float oracle_nvfp4_dynamic_gs(float amax);
+
 /* max_i |v_i| of a dtype tensor (exact), and the calibrated scales. */
 float oracle_amax(int dt, const uint16_t *v, int64_t n);
 float oracle_fp8_scale_from_amax(float amax);    /* f32(amax / 448)  */

@@ -145,3 +145,29 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(rq, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         rq.lib()
+
+
+def test_dynamic_rejections(L):
+    pt = lambda **kw: L.rq_add_rmsnorm_fp8_per_token(
+        kw.get("x", A["x"]), kw.get("r", A["r"]), kw.get("ro", A["ro"]), kw.get("w", A["w"]), 1e-6,
+        kw.get("q", A["q"]), kw.get("sc", A["s"]), kw.get("y", A["y"]), kw.get("rows", 16),
+        kw.get("hidden", 128), 0, None)
+    assert pt(rows=0, x=None) == OK
+    assert pt(sc=None) == NULL
+    assert pt(sc=A["s"] + 2) == MISAL
+    assert pt(sc=A["q"] + 64) == ALIAS  # row scales inside the codes
+    assert pt(hidden=40) == SHAPE
+    dyn = lambda **kw: L.rq_add_rmsnorm_fp8_dynamic(
+        kw.get("x", A["x"]), kw.get("r", A["r"]), kw.get("ro", A["ro"]), kw.get("w", A["w"]), 1e-6,
+        kw.get("sc", A["s"]), kw.get("q", A["q"]), kw.get("y", None), kw.get("rows", 16), 128, 0,
+        None)
+    assert dyn(sc=None) == NULL
+    assert dyn(sc=A["s"] + 1) == MISAL
+    assert dyn(q=None) == NULL
+    assert dyn(sc=A["ro"] + 32) == ALIAS
+    nv = lambda **kw: L.rq_add_rmsnorm_nvfp4_dynamic(
+        A["x"], A["r"], A["ro"], A["w"], 1e-6, kw.get("gs", A["s"]), A["q"], kw.get("sf", A["sf"]),
+        None, 16, 128, 1, None)
+    assert nv(sf=None) == NULL
+    assert nv(sf=A["sf"] + 4) == MISAL
+    assert nv(gs=A["sf"]) == ALIAS

@@ -163,3 +163,31 @@ def test_amax_and_scales():
     assert a == np.max(np.abs(pins.bf16_bits_to_f64(y)))
     assert O.fp8_scale_from_amax(a) == float(np.float32(a) / np.float32(448.0))
     assert O.nvfp4_gs_from_amax(a) == float(np.float32(2688.0) / np.float32(a))
+
+
+# ------------------------------------------------------------- dynamic scales
+@pytest.mark.parametrize("dt", ["bf16", "fp16"])
+def test_per_row_scales_are_row_amax_over_448(dt):
+    """Per-token FP8: each row's scale is amax(|y_row|)/448 in fp32, the row's
+    largest magnitude maps to code 0x7E (448) and every code is the nearest
+    E4M3 of y/scale; an all-zero row gets scale 1 and zero codes."""
+    x, r, w = synth.rows_input(21, 40, 512, dt, res_std=2.0)
+    x[3] = 0
+    r[3] = 0
+    _, y = O.add_rmsnorm(dt, x, r, w, 1e-6)
+    q, sc = O.quant_fp8_per_row(dt, y)
+    yv = pins.bits_to_f64(y, dt)
+    amax = np.abs(yv).max(axis=1).astype(np.float32)
+    expect = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    assert np.array_equal(sc, expect)
+    assert sc[3] == 1.0 and np.all((q[3] & 0x7F) == 0)
+    v = (yv.astype(np.float32) / sc[:, None]).astype(np.float64)
+    assert np.array_equal(q, pins.brute_e4m3(v))
+    nz = amax > 0
+    assert np.all(np.max(q[nz] & 0x7F, axis=1) == 0x7E)
+
+
+def test_dynamic_tensor_scales():
+    assert O.fp8_dynamic_scale(0.0) == 1.0 and O.nvfp4_dynamic_gs(0.0) == 1.0
+    assert O.fp8_dynamic_scale(4.48) == float(np.float32(4.48) / np.float32(448.0))
+    assert O.nvfp4_dynamic_gs(6.0) == 448.0
