@@ -278,6 +278,7 @@ def run_ours(args):
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(args, wl, ws)
     next_rows = measure_next_rows(wl, peak_kind_gbs=peaks()[0])
+    small = measure_small_configs(wl)
 
     peak, peak_kind = peaks()
     kernels = {}
@@ -324,6 +325,7 @@ def run_ours(args):
                      "traffic": traffic, "alg_bytes": dbytes},
         "e2e": e2e,
         "next_rows": next_rows,
+        "small_configs": small,
         "gpu_launches": len(calls) * args.steps,
         "clocks": clk.summary(),
     }
@@ -337,9 +339,10 @@ def run_ours(args):
 
 
 def measure_next_rows(wl, peak_kind_gbs, iters=50):
-    """Dynamic-scale calls (timed on their own, outside the step): per-token
-    FP8 on the prefill workload and per-tensor dynamic FP8 / NVFP4 (amax pass +
-    fused pass) on the prefill / large NVFP4 workloads."""
+    """Calls beyond the step, timed on their own: per-token FP8 on the prefill
+    workload, per-tensor dynamic FP8 / NVFP4 (amax pass + fused pass) on the
+    prefill / large NVFP4 workloads, and the Q/K call storing K into a KV pool
+    of 8192 slots at shuffled slot indices."""
     rq, d = wl.rq, wl.d
     f = lambda: torch.zeros(1, dtype=torch.float32, device="cuda")
     row_scales = torch.empty(FP8_ROWS, dtype=torch.float32, device="cuda")
@@ -357,6 +360,14 @@ def measure_next_rows(wl, peak_kind_gbs, iters=50):
          lambda: rq.rq_add_rmsnorm_nvfp4_dynamic(d["x5"], d["r5"], wl.ro5, wl.w5, EPS, g5, wl.p5,
                                                  wl.sf5, wl.y5)),
     ]
+    n_slots = 2 * QK_T
+    pool = torch.empty((n_slots, QK_HK, QK_D), dtype=torch.uint8, device="cuda")
+    slots = torch.randperm(n_slots, generator=torch.Generator().manual_seed(0))[:QK_T].cuda()
+    cases.append(("qk_rmsnorm_rope_fp8_kv_store", QK_T * (QK_HQ + QK_HK),
+                  alg_bytes_qk(QK_T, QK_HQ, QK_HK, QK_D) + QK_T * 8,
+                  lambda: rq.rq_qk_rmsnorm_rope_fp8_kv_store(d["q4"], d["k4"], wl.qw4, wl.kw4, EPS,
+                                                             d["pos4"], wl.cs4, wl.qs4, wl.ks4,
+                                                             wl.qo4, pool, slots)))
     out = {}
     stream = torch.cuda.current_stream()
     for name, rows, nbytes, fn in cases:
@@ -380,6 +391,74 @@ def measure_next_rows(wl, peak_kind_gbs, iters=50):
 
 
 IN_KEYS = {"fp8": ("x3", "r3"), "qk": ("q4", "k4", "pos4"), "nvfp4": ("x5", "r5")}
+
+
+def measure_small_configs(wl, reps=30, graph_len=20):
+    """Latency of the small workloads, which are launch- and latency-bound:
+    cold = one launch right after an L2 flush (a 512 MB fill queued ahead, so
+    the event brackets only the kernel); warm = a CUDA graph of graph_len
+    back-to-back launches on L2-resident data, per launch."""
+    rq = wl.rq
+    out = {}
+    u8 = dict(dtype=torch.uint8, device="cuda")
+    x1, r1, w1 = synth.rows_input(0, 16, 128, "bf16")
+    x1, r1, w1 = dev16(x1).cuda(), dev16(r1).cuda(), dev16(w1).cuda()
+    s1 = torch.tensor([0.05], dtype=torch.float32, device="cuda")
+    ro1, q1 = torch.empty_like(r1), torch.empty((16, 128), **u8)
+    x2, r2, w2 = synth.rows_input(0, 64, 8192, "fp16")
+    f16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.float16).cuda()
+    x2, r2, w2 = f16(x2), f16(r2), f16(w2)
+    a2 = torch.zeros(1, dtype=torch.float32, device="cuda")
+    g2 = torch.zeros(1, dtype=torch.float32, device="cuda")
+    rq.rq_add_rmsnorm_amax(x2, r2, w2, EPS, a2)
+    rq.rq_nvfp4_global_scale_from_amax(a2, g2)
+    ro2, y2 = torch.empty_like(r2), torch.empty_like(x2)
+    p2, sf2 = torch.empty((64, 4096), **u8), torch.empty((64, 512), **u8)
+    cases = [
+        ("tiny_fp8_16x128_bf16", 16, alg_bytes_fp8(16, 128),
+         lambda: rq.rq_add_rmsnorm_fp8(x1, r1, ro1, w1, EPS, s1, q1)),
+        ("nvfp4_tail_64x8192_fp16_norm_out", 64, alg_bytes_nvfp4(64, 8192),
+         lambda: rq.rq_add_rmsnorm_nvfp4(x2, r2, ro2, w2, EPS, g2, p2, sf2, y2)),
+        ("qk_4096tok_16q8k_bf16", QK_T * (QK_HQ + QK_HK), alg_bytes_qk(QK_T, QK_HQ, QK_HK, QK_D), wl.qk),
+    ]
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    for name, rows, nbytes, fn in cases:
+        fn()
+        torch.cuda.synchronize()
+        cold = []
+        for i in range(reps):
+            flush.fill_(i & 0xFF)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            cold.append((a, b))
+        torch.cuda.synchronize()
+        cold_us = statistics.median(a.elapsed_time(b) * 1e3 for a, b in cold)
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            fn()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            for _ in range(graph_len):
+                fn()
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        warm_us = a.elapsed_time(b) * 1e3 / (reps * graph_len)
+        out[name] = {"cold_us": round(cold_us, 2), "warm_graph_us": round(warm_us, 2),
+                     "alg_bytes": nbytes, "rows_per_s_cold": rows / (cold_us * 1e-6),
+                     "gbs_cold": round(nbytes / (cold_us * 1e-6) / 1e9, 1)}
+    return out
 
 
 def run_e2e(args, wl, ws):

@@ -146,6 +146,26 @@ rq_status rq_qk_rmsnorm_rope_fp8(const void *q, const void *k,
                                  rq_stream_t stream);
 
 /*
+ * The same Q/K call with K's codes stored into a KV-cache pool instead of a
+ * dense tensor: token t's K heads go to pool row k_slots[t] of
+ * k_pool[num_slots, n_k_heads, head_dim] (E4M3 bytes).  A slot outside
+ * [0, num_slots) (e.g. -1 for a padding token) stores nothing for that
+ * token.  Q is written densely to q_out as above.
+ * Source: "perf: add fused norm + RoPE + uniform fp8 store for TRT-LLM DSv4
+ * sparse attention" (SGLang PR 32975), review thread: the norm + RoPE kernel
+ * with a store epilogue into a uniform FP8 KV pool.
+ *   k_slots   [n_tokens] int64 (8-byte aligned); required when n_k_heads > 0
+ */
+rq_status rq_qk_rmsnorm_rope_fp8_kv_store(
+    const void *q, const void *k, int64_t q_token_stride,
+    int64_t k_token_stride, int64_t n_tokens, int n_q_heads, int n_k_heads,
+    int head_dim, const void *q_weight, const void *k_weight, float eps,
+    const int32_t *positions, const float *cos_sin_cache, int64_t max_pos,
+    const float *d_q_scale, const float *d_k_scale, uint8_t *q_out,
+    uint8_t *k_pool, const int64_t *k_slots, int64_t num_slots, rq_dtype dt,
+    rq_stream_t stream);
+
+/*
  * Calibration: d_amax = max over the tensor of |y| (the norm output the
  * fused calls would produce), written to one device fp32.  Nothing else is
  * written.  The call clears d_amax on `stream` first (so an empty tensor

@@ -30,6 +30,9 @@ SIGNATURES = {
                                     _int, _vp]),
     "rq_qk_rmsnorm_rope_fp8": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp, _vp,
                                       _f32, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _int, _vp]),
+    "rq_qk_rmsnorm_rope_fp8_kv_store": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp,
+                                               _vp, _f32, _vp, _vp, _i64, _vp, _vp, _vp, _vp,
+                                               _vp, _i64, _int, _vp]),
     "rq_add_rmsnorm_amax": (_int, [_vp, _vp, _vp, _f32, _vp, _i64, _i64, _int, _vp]),
     "rq_add_rmsnorm_fp8_per_token": (_int, [_vp, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _i64, _i64,
                                             _int, _vp]),
@@ -203,6 +206,22 @@ def rq_qk_rmsnorm_rope_fp8(q, k, q_weight, k_weight, eps, positions, cos_sin_cac
         _ptr(k_weight), float(eps), _ptr(positions), _ptr(cos_sin_cache),
         cos_sin_cache.shape[0], _ptr(q_scale), _ptr(k_scale), _ptr(q_out), _ptr(k_out),
         _dt(ref), _stream(stream)))
+
+
+def rq_qk_rmsnorm_rope_fp8_kv_store(q, k, q_weight, k_weight, eps, positions, cos_sin_cache,
+                                    q_scale, k_scale, q_out, k_pool, k_slots, stream=None):
+    """Q/K RMSNorm + RoPE + FP8 with K stored into a KV pool (include/rq.h):
+    k_pool uint8 [num_slots, n_k_heads, 128]; k_slots int64 [n_tokens]."""
+    tq, hq, sq = _heads(q)
+    tk, hk, sk = _heads(k)
+    ref = q if q is not None else k
+    if q is not None and k is not None and (tq != tk or q.dtype != k.dtype):
+        raise ValueError("q and k must have the same token count and dtype")
+    _check(lib().rq_qk_rmsnorm_rope_fp8_kv_store(
+        _ptr(q), _ptr(k), sq, sk, ref.shape[0], hq, hk, ref.shape[2], _ptr(q_weight),
+        _ptr(k_weight), float(eps), _ptr(positions), _ptr(cos_sin_cache), cos_sin_cache.shape[0],
+        _ptr(q_scale), _ptr(k_scale), _ptr(q_out), _ptr(k_pool), _ptr(k_slots),
+        0 if k_pool is None else k_pool.shape[0], _dt(ref), _stream(stream)))
 
 
 def rq_nvfp4_packed_bytes(rows, hidden):

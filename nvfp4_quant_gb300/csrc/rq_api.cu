@@ -286,13 +286,15 @@ rq_status rq_add_rmsnorm_nvfp4_dynamic(const void *x, const void *residual_in, v
                                                rows, hidden, dt, stream);
 }
 
-rq_status rq_qk_rmsnorm_rope_fp8(const void *q, const void *k, int64_t q_token_stride,
-                                 int64_t k_token_stride, int64_t n_tokens, int n_q_heads,
-                                 int n_k_heads, int head_dim, const void *q_weight,
-                                 const void *k_weight, float eps, const int32_t *positions,
-                                 const float *cos_sin_cache, int64_t max_pos,
-                                 const float *d_q_scale, const float *d_k_scale, uint8_t *q_out,
-                                 uint8_t *k_out, rq_dtype dt, rq_stream_t stream)
+}  // extern "C"
+
+static rq_status qk_call(const void *q, const void *k, int64_t q_token_stride,
+                         int64_t k_token_stride, int64_t n_tokens, int n_q_heads, int n_k_heads,
+                         int head_dim, const void *q_weight, const void *k_weight, float eps,
+                         const int32_t *positions, const float *cos_sin_cache, int64_t max_pos,
+                         const float *d_q_scale, const float *d_k_scale, uint8_t *q_out,
+                         uint8_t *k_out, const int64_t *k_slots, int64_t num_slots, rq_dtype dt,
+                         rq_stream_t stream)
 {
     if (dt != RQ_BF16 && dt != RQ_FP16) return RQ_ERR_DTYPE;
     if (n_tokens < 0 || n_q_heads < 0 || n_k_heads < 0 || max_pos < 1 || n_tokens > (int64_t)1 << 36)
@@ -307,7 +309,10 @@ rq_status rq_qk_rmsnorm_rope_fp8(const void *q, const void *k, int64_t q_token_s
     if (!positions || !cos_sin_cache) return RQ_ERR_NULL;
     if (has_q && (!q || !q_weight || !d_q_scale || !q_out)) return RQ_ERR_NULL;
     if (has_k && (!k || !k_weight || !d_k_scale || !k_out)) return RQ_ERR_NULL;
-    if (!aligned16(cos_sin_cache) || !aligned4(positions)) return RQ_ERR_MISALIGNED;
+    if (k_slots && has_k && num_slots < 0) return RQ_ERR_SHAPE;
+    if (!aligned16(cos_sin_cache) || !aligned4(positions) ||
+        (k_slots && (reinterpret_cast<uintptr_t>(k_slots) & 7u)))
+        return RQ_ERR_MISALIGNED;
     if (has_q && (!aligned16(q) || !aligned16(q_weight) || !aligned16(q_out) || !aligned4(d_q_scale)))
         return RQ_ERR_MISALIGNED;
     if (has_k && (!aligned16(k) || !aligned16(k_weight) || !aligned16(k_out) || !aligned4(d_k_scale)))
@@ -315,14 +320,16 @@ rq_status rq_qk_rmsnorm_rope_fp8(const void *q, const void *k, int64_t q_token_s
     // input extents: the last token's heads end before (T-1)*stride + H*D
     const int64_t qin = has_q && n_tokens > 0 ? ((n_tokens - 1) * q_token_stride + (int64_t)n_q_heads * head_dim) * 2 : 0;
     const int64_t kin = has_k && n_tokens > 0 ? ((n_tokens - 1) * k_token_stride + (int64_t)n_k_heads * head_dim) * 2 : 0;
+    const int64_t k_rows = k_slots ? num_slots : n_tokens;
     const Span ins[] = {span(has_q ? q : nullptr, qin), span(has_k ? k : nullptr, kin),
                         span(has_q ? q_weight : nullptr, head_dim * 2),
                         span(has_k ? k_weight : nullptr, head_dim * 2), span(positions, n_tokens * 4),
                         span(cos_sin_cache, max_pos * head_dim * 4),
-                        span(has_q ? d_q_scale : nullptr, 4), span(has_k ? d_k_scale : nullptr, 4)};
+                        span(has_q ? d_q_scale : nullptr, 4), span(has_k ? d_k_scale : nullptr, 4),
+                        span(has_k ? k_slots : nullptr, n_tokens * 8)};
     const Span outs[] = {span(has_q ? q_out : nullptr, n_tokens * n_q_heads * (int64_t)head_dim),
-                         span(has_k ? k_out : nullptr, n_tokens * n_k_heads * (int64_t)head_dim)};
-    if (bad_alias(outs, 2, ins, 8)) return RQ_ERR_ALIAS;
+                         span(has_k ? k_out : nullptr, k_rows * n_k_heads * (int64_t)head_dim)};
+    if (bad_alias(outs, 2, ins, 9)) return RQ_ERR_ALIAS;
 
     rq::QKParams p;
     p.q = q;
@@ -342,10 +349,43 @@ rq_status rq_qk_rmsnorm_rope_fp8(const void *q, const void *k, int64_t q_token_s
     p.k_scale = d_k_scale;
     p.q_out = q_out;
     p.k_out = k_out;
+    p.k_slots = has_k ? k_slots : nullptr;
+    p.num_slots = num_slots;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = dt == RQ_BF16 ? rq::launch_qk_rmsnorm_rope_fp8<rq::BF16>(p, s)
                                   : rq::launch_qk_rmsnorm_rope_fp8<rq::FP16>(p, s);
     return cuda_status(e);
+}
+
+extern "C" {
+
+rq_status rq_qk_rmsnorm_rope_fp8(const void *q, const void *k, int64_t q_token_stride,
+                                 int64_t k_token_stride, int64_t n_tokens, int n_q_heads,
+                                 int n_k_heads, int head_dim, const void *q_weight,
+                                 const void *k_weight, float eps, const int32_t *positions,
+                                 const float *cos_sin_cache, int64_t max_pos,
+                                 const float *d_q_scale, const float *d_k_scale, uint8_t *q_out,
+                                 uint8_t *k_out, rq_dtype dt, rq_stream_t stream)
+{
+    return qk_call(q, k, q_token_stride, k_token_stride, n_tokens, n_q_heads, n_k_heads, head_dim,
+                   q_weight, k_weight, eps, positions, cos_sin_cache, max_pos, d_q_scale, d_k_scale,
+                   q_out, k_out, nullptr, 0, dt, stream);
+}
+
+rq_status rq_qk_rmsnorm_rope_fp8_kv_store(const void *q, const void *k, int64_t q_token_stride,
+                                          int64_t k_token_stride, int64_t n_tokens, int n_q_heads,
+                                          int n_k_heads, int head_dim, const void *q_weight,
+                                          const void *k_weight, float eps,
+                                          const int32_t *positions, const float *cos_sin_cache,
+                                          int64_t max_pos, const float *d_q_scale,
+                                          const float *d_k_scale, uint8_t *q_out,
+                                          uint8_t *k_pool, const int64_t *k_slots,
+                                          int64_t num_slots, rq_dtype dt, rq_stream_t stream)
+{
+    if (n_k_heads > 0 && n_tokens > 0 && !k_slots) return RQ_ERR_NULL;
+    return qk_call(q, k, q_token_stride, k_token_stride, n_tokens, n_q_heads, n_k_heads, head_dim,
+                   q_weight, k_weight, eps, positions, cos_sin_cache, max_pos, d_q_scale, d_k_scale,
+                   q_out, k_pool, k_slots, num_slots, dt, stream);
 }
 
 size_t rq_nvfp4_packed_bytes(int64_t rows, int64_t hidden)

@@ -44,6 +44,8 @@ struct QKParams {
     const float *k_scale;
     uint8_t *q_out;
     uint8_t *k_out;
+    const int64_t *k_slots;  // null: K dense [T, Hk, D]; else K goes to pool row k_slots[t]
+    int64_t num_slots;       // rows of the K pool
 };
 
 enum QuantMode { MODE_FP8 = 0, MODE_NVFP4 = 1, MODE_AMAX = 2, MODE_FP8_ROW = 3 };

@@ -70,6 +70,14 @@ __device__ __forceinline__ void qk_body(const QKParams &p)
                             __uint_as_float(s1.z ^ neg), __uint_as_float(s1.w ^ neg)};
         const uint8_t *qtok = static_cast<const uint8_t *>(p.q) + tok * p.q_stride * 2;
         const uint8_t *ktok = static_cast<const uint8_t *>(p.k) + tok * p.k_stride * 2;
+        // K destination row: the token itself, or its slot in the KV pool
+        // (slots outside [0, num_slots) write nothing)
+        int64_t krow = tok;
+        if (p.k_slots != nullptr) {
+            int64_t sl;
+            asm volatile("ld.global.nc.s64 %0, [%1];" : "=l"(sl) : "l"(p.k_slots + tok));
+            krow = (sl >= 0 && sl < p.num_slots) ? sl : -1;
+        }
 
         {
             uint4 xv[kPairs];
@@ -118,9 +126,9 @@ __device__ __forceinline__ void qk_body(const QKParams &p)
 #pragma unroll
                 for (int e = 0; e < 8; ++e) v[e] = div_by<kFast>(o[e], by);
                 const uint2 code = e4m3x8(v);
-                if (h < heads) {
+                if (h < heads && (is_q || krow >= 0)) {
                     uint8_t *dst = is_q ? p.q_out + (tok * p.hq + h) * kHeadDim
-                                        : p.k_out + (tok * p.hk + (h - p.hq)) * kHeadDim;
+                                        : p.k_out + (krow * p.hk + (h - p.hq)) * kHeadDim;
                     st8(dst + lane16 * 8, code.x, code.y);
                 }
             }

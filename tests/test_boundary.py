@@ -171,3 +171,15 @@ def test_dynamic_rejections(L):
     assert nv(sf=None) == NULL
     assert nv(sf=A["sf"] + 4) == MISAL
     assert nv(gs=A["sf"]) == ALIAS
+
+
+def test_kv_store_rejections(L):
+    f = lambda **kw: L.rq_qk_rmsnorm_rope_fp8_kv_store(
+        A["x"], A["k"], 16 * 128, 8 * 128, kw.get("T", 32), 16, kw.get("hk", 8), 128, A["w"], A["r"],
+        1e-6, A["pos"], A["cs"], 4096, A["qs"], A["ks"], A["qo"], kw.get("pool", A["ko"]),
+        kw.get("slots", A["y"]), kw.get("ns", 100), 0, None)
+    assert f(slots=None) == NULL
+    assert f(slots=A["y"] + 4) == MISAL
+    assert f(ns=-1) == SHAPE
+    assert f(pool=A["y"]) == ALIAS  # pool over the slot indices
+    assert f(T=0, slots=None) == OK

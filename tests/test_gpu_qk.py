@@ -128,3 +128,33 @@ def test_qk_position_zero_matches_row_norm_kernel():
     rq.rq_add_rmsnorm_fp8(x, r, r, dev16(qw, "bf16"), 1e-6, f32dev(0.01), codes)
     torch.cuda.synchronize()
     assert_codes(qq.reshape(T * Hq, D), host8(codes), 0x80, "Q codes vs row kernel")
+
+
+@pytest.mark.parametrize("dt", ["bf16", "fp16"])
+def test_kv_pool_store(dt):
+    """K codes land in pool rows k_slots[t]; slots outside the pool (padding)
+    write nothing, other pool rows keep their bytes; Q is dense as usual."""
+    T, Hq, Hk, n_slots = 300, 8, 4, 1000
+    q, k, qw, kw, pos, cs = synth.qk_input(7, T, Hq, Hk, D, dt)
+    rng = np.random.default_rng(7)
+    slots = rng.permutation(n_slots)[:T].astype(np.int64)
+    slots[::17] = -1
+    slots[5] = n_slots + 3  # outside the pool: skipped
+    _, qq_ref = O.qk_rmsnorm_rope_fp8(dt, q.reshape(-1), Hq * D, T, Hq, D, qw, 1e-6, pos, cs, 0.02)
+    _, kq_ref = O.qk_rmsnorm_rope_fp8(dt, k.reshape(-1), Hk * D, T, Hk, D, kw, 1e-6, pos, cs, 0.03)
+    pool_ref = np.full((n_slots, Hk, D), 0x5A, np.uint8)
+    ok = (slots >= 0) & (slots < n_slots)
+    pool_ref[slots[ok]] = kq_ref[ok]
+    pool = torch.full((n_slots, Hk, D), 0x5A, dtype=torch.uint8, device="cuda")
+    qo = torch.empty((T, Hq, D), dtype=torch.uint8, device="cuda")
+    rq.rq_qk_rmsnorm_rope_fp8_kv_store(dev16(q, dt), dev16(k, dt), dev16(qw, dt), dev16(kw, dt),
+                                       1e-6, torch.from_numpy(pos).cuda(),
+                                       torch.from_numpy(cs).cuda(), f32dev(0.02), f32dev(0.03),
+                                       qo, pool, torch.from_numpy(slots).cuda())
+    torch.cuda.synchronize()
+    assert_codes(host8(qo), qq_ref, 0x80, "Q codes")
+    got = host8(pool)
+    untouched = np.ones(n_slots, bool)
+    untouched[slots[ok]] = False
+    assert np.all(got[untouched] == 0x5A)
+    assert_codes(got[~untouched], pool_ref[~untouched], 0x80, "K pool codes")
