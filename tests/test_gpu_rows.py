@@ -292,3 +292,25 @@ def test_streams_are_honoured():
         rq.rq_add_rmsnorm_fp8(xd, rd, rd, wd, 1e-6, f32dev(0.02), q, stream=s)
     s.synchronize()
     assert_codes(host8(q), q_ref, 0x80, "FP8 codes on a side stream")
+
+
+@pytest.mark.parametrize("dt", ["bf16", "fp16"])
+def test_fp8_codes_exact_for_every_value_at_many_scales(dt):
+    """The kernels form y / scale by one multiply when a per-CTA check shows
+    that this gives the same E4M3 code as the IEEE quotient for every value of
+    the dtype, else by an exact division.  Either way the codes must equal
+    the oracle's for every finite dtype value, at any scale."""
+    b = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    v = pins.bits_to_f64(b, dt)
+    vals = b[np.isfinite(v)]
+    H = 8192
+    vals = np.concatenate([vals, np.zeros((-vals.size) % H, np.uint16)]).reshape(-1, H)
+    rng = np.random.default_rng(123)
+    scales = np.exp(rng.uniform(np.log(1e-6), np.log(1e4), 48)).astype(np.float32)
+    ones = pins.f64_to_dt(np.ones((1, H)), dt)
+    for scale in scales:
+        for w in vals:
+            s_ref, y_ref, q_ref = O.add_rmsnorm_fp8(dt, ones, np.zeros_like(ones), w, 0.0, float(scale))
+            _, y, q = run_fp8(dt, ones, np.zeros_like(ones), w, 0.0, float(scale), norm_out=True)
+            assert np.array_equal(y, y_ref)
+            assert np.array_equal(q, q_ref), "E4M3 codes differ at scale %r" % float(scale)
