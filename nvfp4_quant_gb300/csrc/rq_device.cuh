@@ -70,8 +70,6 @@ __device__ __forceinline__ void st1(void *p, uint32_t v)
 // A 32-bit word holds two 16-bit elements, the lower-addressed one in the
 // low half.  Unpacking is exact; packing rounds to nearest even.
 struct BF16 {
-    static __device__ __forceinline__ float floor_pos(float v);
-    static __device__ __forceinline__ float next_up(float c);
     static __device__ __forceinline__ float lo(uint32_t u) { return __uint_as_float(u << 16); }
     static __device__ __forceinline__ float hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
     static __device__ __forceinline__ uint32_t pack(float lo_v, float hi_v)
@@ -83,8 +81,6 @@ struct BF16 {
 };
 
 struct FP16 {
-    static __device__ __forceinline__ float floor_pos(float v);
-    static __device__ __forceinline__ float next_up(float c);
     static __device__ __forceinline__ float lo(uint32_t u)
     {
         float f;
@@ -178,36 +174,6 @@ __device__ __forceinline__ float e4m3_value(uint32_t byte)
     return f;
 }
 
-// ---------------------------------------------------------------- dtype neighbours
-// Largest dtype value <= v (v >= 0, finite or +inf) and the next dtype value
-// above a dtype value, as floats (inf past the largest finite).
-__device__ __forceinline__ float bf16_floor(float v)
-{
-    uint32_t h;
-    asm("{ .reg .b16 t; cvt.rz.bf16.f32 t, %1; cvt.u32.u16 %0, t; }" : "=r"(h) : "f"(v));
-    return __uint_as_float(h << 16);
-}
-__device__ __forceinline__ float bf16_next_up(float c) { return __uint_as_float(__float_as_uint(c) + 0x10000u); }
-__device__ __forceinline__ float fp16_floor(float v)
-{
-    float f;
-    asm("{ .reg .b16 t; cvt.rz.f16.f32 t, %1; cvt.f32.f16 %0, t; }" : "=f"(f) : "f"(v));
-    return f;
-}
-__device__ __forceinline__ float fp16_next_up(float c)
-{
-    uint32_t h;
-    float f;
-    asm("{ .reg .b16 t; cvt.rn.f16.f32 t, %1; cvt.u32.u16 %0, t; }" : "=r"(h) : "f"(c));
-    asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.f32.f16 %0, t; }" : "=f"(f) : "r"(h + 1u));
-    return f;
-}
-
-__device__ __forceinline__ float BF16::floor_pos(float v) { return bf16_floor(v); }
-__device__ __forceinline__ float BF16::next_up(float c) { return bf16_next_up(c); }
-__device__ __forceinline__ float FP16::floor_pos(float v) { return fp16_floor(v); }
-__device__ __forceinline__ float FP16::next_up(float c) { return fp16_next_up(c); }
-
 // ---------------------------------------------------------------- division
 // IEEE single operations, round to nearest even (PTX rcp.rn / div.rn are the
 // correctly rounded reciprocal and quotient).
@@ -252,19 +218,9 @@ __device__ __forceinline__ float fma_rn(float a, float b, float c)
 //     signed zero);
 //   * signed zeros keep their sign, a NaN dividend gives NaN, an infinite one
 //     2^20 (E4M3: 448, as satfinite gives for infinity).
-// Divisors outside [2^-40, 2^40] (or not positive) must use the IEEE division.
-//
-// For an E4M3 destination there is a cheaper exact case: E4M3(RN(v * y))
-// equals E4M3(RN(v / b)) for every value v of the input dtype unless one of
-// those v lies within about an fp32 ulp (relative 2^-22) of M * b for an
-// E4M3 rounding boundary M (the 126 midpoints between consecutive E4M3
-// magnitudes; both sides are monotone in v, are within one ulp of each other,
-// and map to 448 from 448 up).  Only the dtype values just below and just
-// above M * b can be that close, so checking those 252 values decides the
-// whole dtype; e4m3_mul_is_exact does that once per CTA.  Kernels then use
-//   DIV_MUL        one multiply by y (the check passed),
-//   DIV_MARKSTEIN  the branch-free correctly rounded division above,
-//   DIV_IEEE       div.rn (divisor outside the fast range).
+// Divisors outside [2^-40, 2^40] (or not positive) must use the IEEE division:
+// kernels test Divisor::fast once and run a body instantiated with
+// kFast = false for them, so the per-element path has no branch.
 struct Divisor {
     float b, y, clamp;
     bool fast;
@@ -274,40 +230,15 @@ struct Divisor {
     }
 };
 
-enum DivMode { DIV_MUL = 0, DIV_MARKSTEIN = 1, DIV_IEEE = 2 };
-
-template <int kMode>
+template <bool kFast>
 __device__ __forceinline__ float div_by(float a, const Divisor &d)
 {
-    if (kMode == DIV_MUL) return mul_rn(a, d.y);
-    if (kMode == DIV_IEEE) return div_rn(a, d.b);
+    if (!kFast) return div_rn(a, d.b);
     float m;
     asm("{ .reg .f32 t; abs.f32 t, %1; min.NaN.f32 %0, t, %2; }" : "=f"(m) : "f"(a), "f"(d.clamp));
     const float q = mul_rn(m, d.y);
     const float r = fma_rn(-q, d.b, m);
     return copysignf(fma_rn(r, d.y, q), a);
-}
-
-// True (in every thread of the CTA) when one multiply by d.y gives the E4M3
-// code of the correctly rounded quotient for every value of the dtype DT (see
-// above).  All threads of the CTA must call it.
-template <typename DT>
-__device__ __forceinline__ bool e4m3_mul_is_exact(const Divisor &d)
-{
-    int bad = !d.fast;
-    for (int i = threadIdx.x; !bad && i < 2 * 126; i += blockDim.x) {
-        const uint32_t m = (uint32_t)i >> 1;
-        const float mid = 0.5f * (e4m3_value(m) + e4m3_value(m + 1));  // exact: <= 5 bits
-        const float v = mul_rn(mid, d.b);
-        float c = DT::floor_pos(v);
-        if (i & 1) c = DT::next_up(c);
-        if (c == c && c < __int_as_float(0x7f800000)) {  // finite
-            const uint32_t c_mul = e4m3x2(mul_rn(c, d.y), 0.0f) & 0xFFu;
-            const uint32_t c_div = e4m3x2(div_rn(c, d.b), 0.0f) & 0xFFu;
-            bad |= c_mul != c_div;
-        }
-    }
-    return __syncthreads_or(bad) == 0;
 }
 
 // ---------------------------------------------------------------- reductions

@@ -36,9 +36,9 @@ struct GroupShape {
     static constexpr int kWarpsPerGroup = G > 32 ? G / 32 : 1;
 };
 
-// kDiv: how the FP8 quotient y / scale is formed (DivMode; the kernel picks
-// the body once, see Divisor).
-template <typename DT, int G, int VPT, int MODE, int kDiv>
+// kFast: the FP8 divisor is in the range of the branch-free division (the
+// kernel picks the body once; see Divisor).
+template <typename DT, int G, int VPT, int MODE, bool kFast>
 __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
                                                        float (*red)[GroupShape<G>::kWarps])
 {
@@ -138,7 +138,7 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
             if (MODE == MODE_FP8) {
                 float v[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = div_by<kDiv>(y[e], by_scale);
+                for (int e = 0; e < 8; ++e) v[e] = div_by<kFast>(y[e], by_scale);
                 const uint2 c = e4m3x8(v);
                 if (ok) st8(p.q + row * H + (int64_t)k * 8, c.x, c.y);
             } else if (MODE == MODE_NVFP4) {
@@ -146,7 +146,7 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
 #pragma unroll
                 for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(y[e]));
                 const float a = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));  // 16-element block
-                const float t2 = div_by<DIV_MARKSTEIN>(__fmul_rn(scale, a), by_six);
+                const float t2 = div_by<true>(__fmul_rn(scale, a), by_six);
                 const uint32_t sfc = e4m3x2(t2, 0.0f) & 0xFFu;
                 const float sfv = e4m3_value(sfc);
                 const float enc = sfv == 0.0f ? 0.0f : __fdiv_rn(scale, sfv);
@@ -204,10 +204,10 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
                 unpack8<DT>(sv[j], y);
                 if (d.fast) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) v[e] = div_by<DIV_MARKSTEIN>(y[e], d);
+                    for (int e = 0; e < 8; ++e) v[e] = div_by<true>(y[e], d);
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) v[e] = div_by<DIV_IEEE>(y[e], d);
+                    for (int e = 0; e < 8; ++e) v[e] = div_by<false>(y[e], d);
                 }
                 const uint2 c = e4m3x8(v);
                 if (row_ok && k < nvec) st8(p.q + row * H + (int64_t)k * 8, c.x, c.y);
@@ -235,17 +235,10 @@ __global__ void __launch_bounds__(GroupShape<G>::kBlock)
 add_rmsnorm_quant_kernel(const NormQuantParams p)
 {
     __shared__ float red[2][GroupShape<G>::kWarps];
-    if (MODE == MODE_FP8) {
-        const Divisor d(ld_f32(p.scale));
-        if (e4m3_mul_is_exact<DT>(d))
-            add_rmsnorm_quant_body<DT, G, VPT, MODE, DIV_MUL>(p, red);
-        else if (d.fast)
-            add_rmsnorm_quant_body<DT, G, VPT, MODE, DIV_MARKSTEIN>(p, red);
-        else
-            add_rmsnorm_quant_body<DT, G, VPT, MODE, DIV_IEEE>(p, red);
-    } else {
-        add_rmsnorm_quant_body<DT, G, VPT, MODE, DIV_MARKSTEIN>(p, red);
-    }
+    if (MODE == MODE_FP8 && !Divisor(ld_f32(p.scale)).fast)
+        add_rmsnorm_quant_body<DT, G, VPT, MODE, false>(p, red);
+    else
+        add_rmsnorm_quant_body<DT, G, VPT, MODE, true>(p, red);
 }
 
 }  // namespace rq

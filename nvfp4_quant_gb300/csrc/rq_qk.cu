@@ -30,7 +30,7 @@ constexpr int kQKBlock = 128;
 constexpr int kHeadDim = 128;
 constexpr int kPairs = 4;  // head pairs per step: 8 heads, 4 loads in flight per lane
 
-template <typename DT, int kDiv>
+template <typename DT, bool kFast>
 __device__ __forceinline__ void qk_body(const QKParams &p)
 {
     const int lane16 = threadIdx.x & 15;
@@ -124,7 +124,7 @@ __device__ __forceinline__ void qk_body(const QKParams &p)
                 const Divisor &by = is_q ? by_q : by_k;
                 float v[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = div_by<kDiv>(o[e], by);
+                for (int e = 0; e < 8; ++e) v[e] = div_by<kFast>(o[e], by);
                 const uint2 code = e4m3x8(v);
                 if (h < heads && (is_q || krow >= 0)) {
                     uint8_t *dst = is_q ? p.q_out + (tok * p.hq + h) * kHeadDim
@@ -140,17 +140,12 @@ template <typename DT>
 __global__ void __launch_bounds__(kQKBlock, 6)
 qk_rmsnorm_rope_fp8_kernel(const QKParams p)
 {
-    // the cheapest exact way to form o / scale for both scales (see Divisor)
-    const Divisor dq(p.hq > 0 ? ld_f32(p.q_scale) : 1.0f);
-    const Divisor dk(p.hk > 0 ? ld_f32(p.k_scale) : 1.0f);
-    const bool mul_q = e4m3_mul_is_exact<DT>(dq);
-    const bool mul_k = e4m3_mul_is_exact<DT>(dk);
-    if (mul_q && mul_k)
-        qk_body<DT, DIV_MUL>(p);
-    else if (dq.fast && dk.fast)
-        qk_body<DT, DIV_MARKSTEIN>(p);
+    const bool fast = (p.hq == 0 || Divisor(ld_f32(p.q_scale)).fast) &&
+                      (p.hk == 0 || Divisor(ld_f32(p.k_scale)).fast);
+    if (fast)
+        qk_body<DT, true>(p);
     else
-        qk_body<DT, DIV_IEEE>(p);
+        qk_body<DT, false>(p);
 }
 
 template <typename DT>

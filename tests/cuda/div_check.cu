@@ -22,7 +22,7 @@ __global__ void check(float b)
         const unsigned int bits = (unsigned int)i;
         const float a = __uint_as_float(bits);
         const float ref = __fdiv_rn(a, b);
-        const float got = d.fast ? rq::div_by<rq::DIV_MARKSTEIN>(a, d) : rq::div_by<rq::DIV_IEEE>(a, d);
+        const float got = d.fast ? rq::div_by<true>(a, d) : rq::div_by<false>(a, d);
         const float m = fabsf(ref);
         if (m >= 0x1p-40f && m < 0x1p20f && __float_as_uint(ref) != __float_as_uint(got)) {
             if (atomicAdd(&g_quot_diff, 1ull) == 0) g_first_bad = bits;

@@ -296,10 +296,9 @@ def test_streams_are_honoured():
 
 @pytest.mark.parametrize("dt", ["bf16", "fp16"])
 def test_fp8_codes_exact_for_every_value_at_many_scales(dt):
-    """The kernels form y / scale by one multiply when a per-CTA check shows
-    that this gives the same E4M3 code as the IEEE quotient for every value of
-    the dtype, else by an exact division.  Either way the codes must equal
-    the oracle's for every finite dtype value, at any scale."""
+    """The kernels form y / scale with Markstein's correction step (or div.rn
+    for divisors out of its range); the codes must equal the oracle's IEEE
+    quotient for every finite dtype value, at any scale."""
     b = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
     v = pins.bits_to_f64(b, dt)
     vals = b[np.isfinite(v)]
