@@ -230,8 +230,14 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
     }
 }
 
+// Register budget: the 128-thread shapes with 7 or 8 vectors per thread hold
+// about 167 registers; past 170 only two CTAs fit per SM and the NVFP4 call on
+// 16,384 x 7168 slows from 160 to 195 us, so they are held to three CTAs.
+template <int G, int VPT>
+constexpr int min_ctas_per_sm() { return (G == 128 && VPT >= 7) ? 3 : 1; }
+
 template <typename DT, int G, int VPT, int MODE>
-__global__ void __launch_bounds__(GroupShape<G>::kBlock)
+__global__ void __launch_bounds__(GroupShape<G>::kBlock, (min_ctas_per_sm<G, VPT>()))
 add_rmsnorm_quant_kernel(const NormQuantParams p)
 {
     __shared__ float red[2][GroupShape<G>::kWarps];
