@@ -304,7 +304,7 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "f32",
         "data": "synthetic (seeded splitmix64 normals, rounded to bf16)",
         "config": {
             "workload": "fused norm+quant prologue step: add_rmsnorm_fp8 65536x1024 bf16 + "
@@ -312,6 +312,8 @@ def run_ours(args):
                         "add_rmsnorm_nvfp4 16384x7168 bf16 with bf16 norm out",
             "rows_per_step": ROWS_PER_STEP,
             "row_note": "a Q/K row is one 128-element head of one token",
+            "io": "bf16 in; bf16 residual / norm out, E4M3 and packed E2M1 + E4M3 scales out; "
+                  "every step computed in fp32",
             "alg_bytes_per_step": STEP_BYTES,
             "step_gbs": round(STEP_BYTES / (ms_per_step / 1e3) / 1e9, 1),
             "l2": "no flush: each kernel's inputs were last touched > 1 GB of HBM traffic "
@@ -638,7 +640,7 @@ def run_reference(args):
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded splitmix64 normals)",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded splitmix64 normals)",
         "impl": "reference",
         "config": {"workload": "fused norm+quant prologue step: add_rmsnorm_fp8 65536x1024 bf16 + "
                                "qk_rmsnorm_rope_fp8 4096 tok x (16+8) heads x 128 bf16 + "

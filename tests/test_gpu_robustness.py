@@ -1,0 +1,112 @@
+"""GPU behaviour beyond the numerics: tensors at offsets inside larger
+allocations, CUDA-graph capture, concurrent calls from two host threads on
+their own streams."""
+import threading
+
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_quant_gb300 as rq
+import oracle as O
+import synth
+from nvfp4_quant_gb300 import build as rq_build
+from tests.gpu_util import assert_codes, dev16, f32dev, host8, host16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    rq_build.build()
+    rq.lib()
+
+
+def test_views_at_aligned_offsets():
+    """x, residual and outputs as row slices of larger buffers (16-byte
+    aligned, not allocation-aligned) give the same bytes as dense tensors."""
+    rows, H = 300, 2048
+    x, r, w = synth.rows_input(41, rows, H, "bf16")
+    s_ref, y_ref, p_ref, sf_ref = O.add_rmsnorm_nvfp4("bf16", x, r, w, 1e-6, 300.0)
+    big_x = torch.zeros((rows + 7, H), dtype=torch.bfloat16, device="cuda")
+    big_r = torch.zeros_like(big_x)
+    big_x[3:3 + rows] = dev16(x, "bf16")
+    big_r[5:5 + rows] = dev16(r, "bf16")
+    xv, rv = big_x[3:3 + rows], big_r[5:5 + rows]
+    out = torch.zeros((rows + 2, H), dtype=torch.bfloat16, device="cuda")
+    yv = out[1:1 + rows]
+    pk = torch.zeros((rows + 4, H // 2), dtype=torch.uint8, device="cuda")[2:2 + rows]
+    sf = torch.zeros((rows * (H // 16) + 64,), dtype=torch.uint8, device="cuda")[16:16 + rows * (H // 16)]
+    rq.rq_add_rmsnorm_nvfp4(xv, rv, rv, dev16(w, "bf16"), 1e-6, f32dev(300.0), pk, sf.view(rows, H // 16), yv)
+    torch.cuda.synchronize()
+    assert np.array_equal(host16(rv), s_ref)
+    p_o, sf_o = O.quant_nvfp4("bf16", host16(yv), 300.0)
+    assert np.array_equal(host8(pk), p_o) and np.array_equal(host8(sf).reshape(rows, -1), sf_o)
+    assert np.all(host16(big_r[:5]) == 0) and np.all(host16(big_r[5 + rows:]) == 0)
+
+
+def test_misaligned_view_is_rejected():
+    x = torch.zeros((8, 136), dtype=torch.bfloat16, device="cuda")
+    v = x.view(-1)[4:4 + 7 * 128].view(7, 128)  # 8-byte offset
+    w = torch.ones(128, dtype=torch.bfloat16, device="cuda")
+    q = torch.empty((7, 128), dtype=torch.uint8, device="cuda")
+    with pytest.raises(rq.RQError) as e:
+        rq.rq_add_rmsnorm_fp8(v, v.clone(), torch.empty_like(v.clone()), w, 1e-6, f32dev(1.0), q)
+    assert e.value.status == 4
+
+
+def test_cuda_graph_capture_and_replay():
+    """The calls are stream-ordered and allocate nothing, so they can be
+    captured; replaying the graph on new inputs gives the eager results."""
+    rows, H = 512, 1024
+    x1, r1, w = synth.rows_input(42, rows, H, "bf16")
+    x2, r2, _ = synth.rows_input(43, rows, H, "bf16")
+    xd, rd, wd = dev16(x1, "bf16"), dev16(r1, "bf16"), dev16(w, "bf16")
+    ro = torch.empty_like(rd)
+    q = torch.empty((rows, H), dtype=torch.uint8, device="cuda")
+    sc = f32dev(0.02)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        rq.rq_add_rmsnorm_fp8(xd, rd, ro, wd, 1e-6, sc, q)  # first call: launch set-up
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        rq.rq_add_rmsnorm_fp8(xd, rd, ro, wd, 1e-6, sc, q)
+    for x, r in ((x1, r1), (x2, r2)):
+        xd.copy_(dev16(x, "bf16"))
+        rd.copy_(dev16(r, "bf16"))
+        g.replay()
+        torch.cuda.synchronize()
+        s_ref, _, q_ref = O.add_rmsnorm_fp8("bf16", x, r, w, 1e-6, 0.02)
+        assert np.array_equal(host16(ro), s_ref)
+        assert_codes(host8(q), q_ref, 0x80, "FP8 codes from graph replay")
+
+
+def test_concurrent_calls_from_two_threads():
+    rows, H = 1024, 4096
+    inputs = [synth.rows_input(44 + i, rows, H, "fp16") for i in range(2)]
+    results = [None, None]
+
+    def work(i):
+        torch.cuda.set_device(0)
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            x, r, w = (dev16(a, "fp16") for a in inputs[i])
+            q = torch.empty((rows, H), dtype=torch.uint8, device="cuda")
+            for _ in range(20):
+                rq.rq_add_rmsnorm_fp8(x, r, torch.empty_like(r), w, 1e-6, f32dev(0.03), q, stream=s)
+            s.synchronize()
+            results[i] = host8(q)
+
+    th = [threading.Thread(target=work, args=(i,)) for i in range(2)]
+    for t in th:
+        t.start()
+    for t in th:
+        t.join()
+    for i in range(2):
+        x, r, w = inputs[i]
+        _, _, q_ref = O.add_rmsnorm_fp8("fp16", x, r, w, 1e-6, 0.03)
+        assert_codes(results[i], q_ref, 0x80, "FP8 codes from thread %d" % i)
