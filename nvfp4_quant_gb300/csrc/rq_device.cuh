@@ -66,6 +66,42 @@ __device__ __forceinline__ void st1(void *p, uint32_t v)
     asm volatile("st.global.u8 [%0], %1;" :: "l"(p), "r"(v) : "memory");
 }
 
+// ---------------------------------------------------------------- shared memory
+// Asynchronous 16-byte global -> shared copies (cp.async, bypassing L1).  A
+// thread that stages data only for itself waits with cp.async.wait_group and
+// needs no barrier.
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    uint32_t a;
+    asm("{ .reg .u64 t; cvta.to.shared.u64 t, %1; cvt.u32.u64 %0, t; }" : "=r"(a) : "l"(p));
+    return a;
+}
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_addr(smem)), "l"(gmem)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+
+__device__ __forceinline__ uint4 lds16(const void *smem)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(smem_addr(smem)) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void sts16(void *smem, uint4 v)
+{
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};"
+                 :: "r"(smem_addr(smem)), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
 // ---------------------------------------------------------------- dtypes
 // A 32-bit word holds two 16-bit elements, the lower-addressed one in the
 // low half.  Unpacking is exact; packing rounds to nearest even.

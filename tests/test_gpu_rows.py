@@ -313,3 +313,31 @@ def test_fp8_codes_exact_for_every_value_at_many_scales(dt):
             _, y, q = run_fp8(dt, ones, np.zeros_like(ones), w, 0.0, float(scale), norm_out=True)
             assert np.array_equal(y, y_ref)
             assert np.array_equal(q, q_ref), "E4M3 codes differ at scale %r" % float(scale)
+
+
+# ------------------------------------------------------------- long rows (shared-memory staged)
+@pytest.mark.parametrize("hidden", [8208, 16384, 16400, 20480, 28672])
+@pytest.mark.parametrize("dt", ["bf16", "fp16"])
+def test_long_rows_through_shared_memory(hidden, dt):
+    """Rows above 8192 elements, at least two per SM, run the kernel that
+    stages x and residual in shared memory: FP8, NVFP4, per-token FP8 and the
+    amax calibration against the oracle."""
+    rows = 2 * SMS + 3
+    x, r, w = synth.rows_input(hidden + 7, rows, hidden, dt, res_std=2.0, outlier_frac=0.01)
+    gs, scale = oracle_gs(dt, x, r, w, 1e-6)
+    check_fp8(dt, x, r, w, 1e-6, scale, norm_out=True)
+    check_nvfp4(dt, x, r, w, 1e-6, gs, norm_out=True, in_place=True)
+    _, y_ref = O.add_rmsnorm(dt, x, r, w, 1e-6)
+    xd, rd, wd = dev16(x, dt), dev16(r, dt), dev16(w, dt)
+    q = torch.empty((rows, hidden), dtype=torch.uint8, device="cuda")
+    sc = torch.empty(rows, dtype=torch.float32, device="cuda")
+    y = torch.empty_like(xd)
+    rq.rq_add_rmsnorm_fp8_per_token(xd, rd, torch.empty_like(rd), wd, 1e-6, q, sc, y)
+    amax = f32dev(0.0)
+    rq.rq_add_rmsnorm_amax(xd, rd, wd, 1e-6, amax)
+    torch.cuda.synchronize()
+    q_o, sc_o = O.quant_fp8_per_row(dt, host16(y))
+    assert np.array_equal(host8(q), q_o) and np.array_equal(sc.cpu().numpy(), sc_o)
+    assert_norm_within_ulp(host16(y), y_ref, dt)
+    a_ref = O.amax(dt, y_ref)
+    assert abs(float(amax.item()) - a_ref) <= pins.ulp(np.array([a_ref]), dt)[0]
