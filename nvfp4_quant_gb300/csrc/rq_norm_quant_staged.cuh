@@ -40,18 +40,25 @@ __device__ __forceinline__ void staged_body(const NormQuantParams &p, uint4 *buf
     float amax_acc = 0.0f;
     int parity = 0;
 
-    for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
-        const uint8_t *xrow = static_cast<const uint8_t *>(p.x) + row * H * 2;
-        const uint8_t *rrow = static_cast<const uint8_t *>(p.res_in) + row * H * 2;
-        for (int i = 0; i < iters; ++i) {
-            const int k = i * T + tid;
-            if (k < nvec) {
-                cp_async16(xs + k, xrow + (int64_t)k * 16);
-                cp_async16(rs + k, rrow + (int64_t)k * 16);
+    // the x slots are refilled with the next row as soon as pass 1 has read
+    // them (not in per-token mode, which keeps the rounded y there)
+    constexpr bool kEarlyX = MODE != MODE_FP8_ROW;
+    auto stage = [&](int64_t r, uint4 *dst, const void *src_base) {
+        if (r < p.rows) {
+            const uint8_t *src = static_cast<const uint8_t *>(src_base) + r * H * 2;
+            for (int i = 0; i < iters; ++i) {
+                const int k = i * T + tid;
+                if (k < nvec) cp_async16(dst + k, src + (int64_t)k * 16);
             }
         }
+    };
+    if (kEarlyX) stage(blockIdx.x, xs, p.x);
+
+    for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
+        if (!kEarlyX) stage(row, xs, p.x);
+        stage(row, rs, p.res_in);
         cp_async_commit();
-        cp_async_wait<0>();  // this thread's own vectors
+        cp_async_wait<0>();  // this thread's own vectors of the row
 
         // ---- pass 1: residual', its squares
         float ss = 0.0f;
@@ -72,6 +79,7 @@ __device__ __forceinline__ void staged_body(const NormQuantParams &p, uint4 *buf
                 for (int e = 0; e < 8; ++e) ss = __fmaf_rn(a[e], a[e], ss);  // squares are exact
             }
         }
+        if (kEarlyX) stage(row + gridDim.x, xs, p.x);  // lands during the rest of this row
         ss = group_sum<32>(ss);
         if ((tid & 31) == 0) red[parity][tid >> 5] = ss;
         __syncthreads();
@@ -168,6 +176,9 @@ __device__ __forceinline__ void staged_body(const NormQuantParams &p, uint4 *buf
             }
         }
     }
+
+    cp_async_commit();
+    cp_async_wait<0>();  // nothing may stay in flight at exit
 
     if (MODE == MODE_AMAX) {
         float m = group_max<32>(amax_acc);
