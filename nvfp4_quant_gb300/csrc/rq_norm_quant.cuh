@@ -233,8 +233,12 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
 // Register budget: the 128-thread shapes with 7 or 8 vectors per thread hold
 // about 167 registers; past 170 only two CTAs fit per SM and the NVFP4 call on
 // 16,384 x 7168 slows from 160 to 195 us, so they are held to three CTAs.
+// Every other shape passes 0 (no minimum), which leaves ptxas its own
+// occupancy heuristic: an explicit minimum of 1 lets it spend up to 255
+// registers, and the 32 x 4 shape went from 96 to 152 registers (five CTAs per
+// SM down to three) and 32,768 x 2048 from 95 to 107 us.
 template <int G, int VPT>
-constexpr int min_ctas_per_sm() { return (G == 128 && VPT >= 7) ? 3 : 1; }
+constexpr int min_ctas_per_sm() { return (G == 128 && VPT >= 7) ? 3 : 0; }
 
 template <typename DT, int G, int VPT, int MODE>
 __global__ void __launch_bounds__(GroupShape<G>::kBlock, (min_ctas_per_sm<G, VPT>()))
