@@ -228,12 +228,49 @@ rq_status rq_add_rmsnorm_nvfp4_dynamic(const void *x, const void *residual_in,
                                        int64_t hidden, rq_dtype dt,
                                        rq_stream_t stream);
 
+/*
+ * The NVFP4 calls with the block scales written in the layout a block-scaled
+ * NVFP4 GEMM reads for an operand (cuBLASLt's 16-element-block / E4M3-scale
+ * mode), so that no reordering pass runs between this call and the GEMM:
+ *   - the rows x (hidden/16) matrix of block scales is padded to a multiple
+ *     of 128 rows and of 4 block columns;
+ *   - it is cut into 128 x 4 tiles of 512 bytes each, stored one row of
+ *     tiles after the other, left to right within a row of tiles;
+ *   - inside a tile, the scale of (row r, block column c) is byte
+ *     16 * (r % 32) + 4 * (r / 32) + c.
+ * Every byte of block_scales is written; the padding bytes are 0.
+ *   block_scales  rq_nvfp4_swizzled_scale_bytes(rows, hidden) bytes
+ * All other arguments, the outputs and the checks are those of
+ * rq_add_rmsnorm_nvfp4 / rq_add_rmsnorm_nvfp4_dynamic; with rows == 0
+ * nothing is written (the padded size is 0 too).
+ * Source: the pages size the scale tensor for its GEMM ("Add AutoDeploy NVFP4
+ * RMSNorm quant fusion", review: the sf_size math of the shape-only ops;
+ * "[Performance]: Fuse local NVFP4 tail after NCCL fallback", Correctness
+ * and build validation: the expected packed NVFP4 output shape) but do not
+ * print the layout; it is the consumer's.
+ */
+rq_status rq_add_rmsnorm_nvfp4_swizzled(const void *x, const void *residual_in,
+                                        void *residual_out, const void *weight,
+                                        float eps, const float *d_global_scale,
+                                        uint8_t *q_packed,
+                                        uint8_t *block_scales, void *norm_out,
+                                        int64_t rows, int64_t hidden,
+                                        rq_dtype dt, rq_stream_t stream);
+rq_status rq_add_rmsnorm_nvfp4_dynamic_swizzled(
+    const void *x, const void *residual_in, void *residual_out,
+    const void *weight, float eps, float *d_global_scale_out,
+    uint8_t *q_packed, uint8_t *block_scales, void *norm_out, int64_t rows,
+    int64_t hidden, rq_dtype dt, rq_stream_t stream);
+
 /* Output sizes of the NVFP4 call (the linear, unswizzled layout):
  * rows * hidden / 2 packed bytes and rows * hidden / 16 scale bytes.
  * Source: "Add AutoDeploy NVFP4 RMSNorm quant fusion", review: the packed
  * output and scale-tensor size math of the fake (shape-only) ops. */
 size_t rq_nvfp4_packed_bytes(int64_t rows, int64_t hidden);
 size_t rq_nvfp4_scale_bytes(int64_t rows, int64_t hidden);
+/* Block-scale bytes of the swizzled calls:
+ * ceil(rows / 128) * 128 * ceil(hidden / 64) * 4. */
+size_t rq_nvfp4_swizzled_scale_bytes(int64_t rows, int64_t hidden);
 
 /* Text of a status code (static storage). */
 const char *rq_status_string(rq_status status);

@@ -44,6 +44,11 @@ SIGNATURES = {
     "rq_nvfp4_global_scale_from_amax": (_int, [_vp, _vp, _vp]),
     "rq_nvfp4_packed_bytes": (ctypes.c_size_t, [_i64, _i64]),
     "rq_nvfp4_scale_bytes": (ctypes.c_size_t, [_i64, _i64]),
+    "rq_add_rmsnorm_nvfp4_swizzled": (_int, [_vp, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _i64,
+                                             _i64, _int, _vp]),
+    "rq_add_rmsnorm_nvfp4_dynamic_swizzled": (_int, [_vp, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _vp,
+                                                     _i64, _i64, _int, _vp]),
+    "rq_nvfp4_swizzled_scale_bytes": (ctypes.c_size_t, [_i64, _i64]),
     "rq_status_string": (ctypes.c_char_p, [_int]),
     "rq_last_error": (ctypes.c_char_p, []),
     "rq_version": (_int, []),
@@ -101,6 +106,13 @@ def _stream(stream):
     return getattr(stream, "cuda_stream", stream)
 
 
+def _out(t, nbytes, name):
+    """An output buffer: contiguous, on x's device, and at least nbytes long
+    (the kernels write exactly the sizes include/rq.h gives)."""
+    if t is None or not t.is_contiguous() or t.numel() * t.element_size() < nbytes:
+        raise ValueError("%s must be a contiguous tensor of at least %d bytes" % (name, nbytes))
+
+
 def _rows(x, *others):
     if x.dim() != 2 or not x.is_contiguous():
         raise ValueError("x must be a contiguous [rows, hidden] tensor")
@@ -117,6 +129,7 @@ def rq_add_rmsnorm_fp8(x, residual_in, residual_out, weight, eps, scale, q_out,
     rows, hidden = _rows(x, residual_in, residual_out, norm_out)
     if weight.dtype != x.dtype:
         raise ValueError("weight dtype must match x")
+    _out(q_out, rows * hidden, "q_out")
     _check(lib().rq_add_rmsnorm_fp8(_ptr(x), _ptr(residual_in), _ptr(residual_out), _ptr(weight),
                                     float(eps), _ptr(scale), _ptr(q_out), _ptr(norm_out),
                                     rows, hidden, _dt(x), _stream(stream)))
@@ -129,6 +142,8 @@ def rq_add_rmsnorm_nvfp4(x, residual_in, residual_out, weight, eps, global_scale
     rows, hidden = _rows(x, residual_in, residual_out, norm_out)
     if weight.dtype != x.dtype:
         raise ValueError("weight dtype must match x")
+    _out(q_packed, rows * hidden // 2, "q_packed")
+    _out(block_scales, rows * (hidden // 16), "block_scales")
     _check(lib().rq_add_rmsnorm_nvfp4(_ptr(x), _ptr(residual_in), _ptr(residual_out),
                                       _ptr(weight), float(eps), _ptr(global_scale),
                                       _ptr(q_packed), _ptr(block_scales), _ptr(norm_out),
@@ -138,6 +153,7 @@ def rq_add_rmsnorm_nvfp4(x, residual_in, residual_out, weight, eps, global_scale
 def rq_add_rmsnorm_amax(x, residual_in, weight, eps, amax_out, stream=None):
     """amax_out[0] = max |RMSNorm(x + residual) * weight| (include/rq.h)."""
     rows, hidden = _rows(x, residual_in)
+    _out(amax_out, 4, "amax_out")
     _check(lib().rq_add_rmsnorm_amax(_ptr(x), _ptr(residual_in), _ptr(weight), float(eps),
                                      _ptr(amax_out), rows, hidden, _dt(x), _stream(stream)))
 
@@ -147,6 +163,8 @@ def rq_add_rmsnorm_fp8_per_token(x, residual_in, residual_out, weight, eps, q_ou
     """Residual add + RMSNorm + FP8 with per-row dynamic scales (include/rq.h).
     row_scales: float32 [rows], written."""
     rows, hidden = _rows(x, residual_in, residual_out, norm_out)
+    _out(q_out, rows * hidden, "q_out")
+    _out(row_scales, rows * 4, "row_scales")
     _check(lib().rq_add_rmsnorm_fp8_per_token(_ptr(x), _ptr(residual_in), _ptr(residual_out),
                                               _ptr(weight), float(eps), _ptr(q_out),
                                               _ptr(row_scales), _ptr(norm_out), rows, hidden,
@@ -158,6 +176,8 @@ def rq_add_rmsnorm_fp8_dynamic(x, residual_in, residual_out, weight, eps, scale_
     """Residual add + RMSNorm + FP8 with the per-tensor scale amax/448 computed
     on the device (include/rq.h); scale_out: 1-element float32, written."""
     rows, hidden = _rows(x, residual_in, residual_out, norm_out)
+    _out(q_out, rows * hidden, "q_out")
+    _out(scale_out, 4, "scale_out")
     _check(lib().rq_add_rmsnorm_fp8_dynamic(_ptr(x), _ptr(residual_in), _ptr(residual_out),
                                             _ptr(weight), float(eps), _ptr(scale_out), _ptr(q_out),
                                             _ptr(norm_out), rows, hidden, _dt(x), _stream(stream)))
@@ -168,10 +188,43 @@ def rq_add_rmsnorm_nvfp4_dynamic(x, residual_in, residual_out, weight, eps, glob
     """Residual add + RMSNorm + NVFP4 with the global scale 2688/amax computed
     on the device (include/rq.h); global_scale_out: 1-element float32, written."""
     rows, hidden = _rows(x, residual_in, residual_out, norm_out)
+    _out(q_packed, rows * hidden // 2, "q_packed")
+    _out(block_scales, rows * (hidden // 16), "block_scales")
+    _out(global_scale_out, 4, "global_scale_out")
     _check(lib().rq_add_rmsnorm_nvfp4_dynamic(_ptr(x), _ptr(residual_in), _ptr(residual_out),
                                               _ptr(weight), float(eps), _ptr(global_scale_out),
                                               _ptr(q_packed), _ptr(block_scales), _ptr(norm_out),
                                               rows, hidden, _dt(x), _stream(stream)))
+
+
+def rq_add_rmsnorm_nvfp4_swizzled(x, residual_in, residual_out, weight, eps, global_scale,
+                                  q_packed, block_scales, norm_out=None, stream=None):
+    """rq_add_rmsnorm_nvfp4 with the block scales in the 128 x 4-tile layout a
+    block-scaled NVFP4 GEMM reads (include/rq.h); block_scales: uint8 of
+    rq_nvfp4_swizzled_scale_bytes(rows, hidden) bytes, every byte written."""
+    rows, hidden = _rows(x, residual_in, residual_out, norm_out)
+    if weight.dtype != x.dtype:
+        raise ValueError("weight dtype must match x")
+    _out(q_packed, rows * hidden // 2, "q_packed")
+    _out(block_scales, rq_nvfp4_swizzled_scale_bytes(rows, hidden), "block_scales")
+    _check(lib().rq_add_rmsnorm_nvfp4_swizzled(_ptr(x), _ptr(residual_in), _ptr(residual_out),
+                                               _ptr(weight), float(eps), _ptr(global_scale),
+                                               _ptr(q_packed), _ptr(block_scales), _ptr(norm_out),
+                                               rows, hidden, _dt(x), _stream(stream)))
+
+
+def rq_add_rmsnorm_nvfp4_dynamic_swizzled(x, residual_in, residual_out, weight, eps,
+                                          global_scale_out, q_packed, block_scales,
+                                          norm_out=None, stream=None):
+    """rq_add_rmsnorm_nvfp4_dynamic with swizzled block scales (include/rq.h)."""
+    rows, hidden = _rows(x, residual_in, residual_out, norm_out)
+    _out(q_packed, rows * hidden // 2, "q_packed")
+    _out(block_scales, rq_nvfp4_swizzled_scale_bytes(rows, hidden), "block_scales")
+    _out(global_scale_out, 4, "global_scale_out")
+    _check(lib().rq_add_rmsnorm_nvfp4_dynamic_swizzled(
+        _ptr(x), _ptr(residual_in), _ptr(residual_out), _ptr(weight), float(eps),
+        _ptr(global_scale_out), _ptr(q_packed), _ptr(block_scales), _ptr(norm_out), rows, hidden,
+        _dt(x), _stream(stream)))
 
 
 def rq_fp8_scale_from_amax(amax, scale_out, stream=None):
@@ -191,6 +244,21 @@ def _heads(t):
     return t.shape[0], t.shape[1], t.stride(0)
 
 
+def _qk_buffers(ref, hq, hk, positions, cos_sin_cache, q_out, k_out):
+    """Sizes of the Q/K call's side inputs and dense outputs (k_out None: pool)."""
+    t, d = ref.shape[0], ref.shape[2]
+    if t == 0:
+        return
+    if positions is None or positions.numel() < t:
+        raise ValueError("positions must hold one int32 per token")
+    if cos_sin_cache is None or cos_sin_cache.dim() != 2 or cos_sin_cache.shape[1] != d:
+        raise ValueError("cos_sin_cache must be a [max_pos, head_dim] float32 tensor")
+    if hq > 0:
+        _out(q_out, t * hq * d, "q_out")
+    if hk > 0 and k_out is not None:
+        _out(k_out, t * hk * d, "k_out")
+
+
 def rq_qk_rmsnorm_rope_fp8(q, k, q_weight, k_weight, eps, positions, cos_sin_cache,
                            q_scale, k_scale, q_out, k_out, stream=None):
     """Per-head Q/K RMSNorm + NeoX RoPE + FP8 E4M3 store (include/rq.h).
@@ -201,6 +269,7 @@ def rq_qk_rmsnorm_rope_fp8(q, k, q_weight, k_weight, eps, positions, cos_sin_cac
     if q is not None and k is not None and (tq != tk or q.dtype != k.dtype):
         raise ValueError("q and k must have the same token count and dtype")
     head_dim = ref.shape[2]
+    _qk_buffers(ref, hq, hk, positions, cos_sin_cache, q_out, k_out)
     _check(lib().rq_qk_rmsnorm_rope_fp8(
         _ptr(q), _ptr(k), sq, sk, ref.shape[0], hq, hk, head_dim, _ptr(q_weight),
         _ptr(k_weight), float(eps), _ptr(positions), _ptr(cos_sin_cache),
@@ -217,6 +286,13 @@ def rq_qk_rmsnorm_rope_fp8_kv_store(q, k, q_weight, k_weight, eps, positions, co
     ref = q if q is not None else k
     if q is not None and k is not None and (tq != tk or q.dtype != k.dtype):
         raise ValueError("q and k must have the same token count and dtype")
+    _qk_buffers(ref, hq, hk, positions, cos_sin_cache, q_out, None)
+    if hk > 0 and ref.shape[0] > 0:
+        if k_pool is None or k_pool.dim() != 3 or k_pool.shape[1:] != (hk, ref.shape[2]) \
+                or not k_pool.is_contiguous():
+            raise ValueError("k_pool must be a contiguous [num_slots, n_k_heads, head_dim] tensor")
+        if k_slots is None or k_slots.dtype != torch.int64 or k_slots.numel() < ref.shape[0]:
+            raise ValueError("k_slots must hold one int64 slot per token")
     _check(lib().rq_qk_rmsnorm_rope_fp8_kv_store(
         _ptr(q), _ptr(k), sq, sk, ref.shape[0], hq, hk, ref.shape[2], _ptr(q_weight),
         _ptr(k_weight), float(eps), _ptr(positions), _ptr(cos_sin_cache), cos_sin_cache.shape[0],
@@ -230,6 +306,10 @@ def rq_nvfp4_packed_bytes(rows, hidden):
 
 def rq_nvfp4_scale_bytes(rows, hidden):
     return int(lib().rq_nvfp4_scale_bytes(rows, hidden))
+
+
+def rq_nvfp4_swizzled_scale_bytes(rows, hidden):
+    return int(lib().rq_nvfp4_swizzled_scale_bytes(rows, hidden))
 
 
 # ---------------------------------------------------------------- conveniences

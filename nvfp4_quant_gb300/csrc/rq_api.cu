@@ -84,7 +84,15 @@ rq::NormQuantParams make_params(const void *x, const void *res_in, void *res_out
     p.rows = rows;
     p.hidden = (int)hidden;
     p.nvec = (int)(hidden / 8);
+    p.sf_col_tiles = (int)((hidden / 16 + 3) / 4);
     return p;
+}
+
+// Bytes of the NVFP4 block scales in either layout.
+int64_t sf_bytes(int64_t rows, int64_t hidden, int swizzled)
+{
+    if (!swizzled) return rows * (hidden / 16);
+    return (rows + 127) / 128 * 128 * ((hidden / 16 + 3) / 4 * 4);
 }
 
 template <int MODE>
@@ -120,12 +128,13 @@ rq_status dynamic_tensor_call(const void *x, const void *residual_in, void *resi
                                      uint8_t *sf, void *norm_out, int64_t rows, int64_t hidden,
                                      rq_dtype dt, rq_stream_t stream)
 {
+    const int sf_swizzled = MODE == rq::MODE_NVFP4_SWZ;
     rq_status st = check_rows(rows, hidden, dt);
     if (st != RQ_OK) return st;
     if (!d_scale_out) return RQ_ERR_NULL;
     if (!aligned4(d_scale_out)) return RQ_ERR_MISALIGNED;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int nvfp4 = MODE == rq::MODE_NVFP4;
+    const int nvfp4 = rq::is_nvfp4<MODE>();
     if (rows > 0) {
         if (!x || !residual_in || !residual_out || !weight || !q || (nvfp4 && !sf)) return RQ_ERR_NULL;
         if (!aligned16(x) || !aligned16(residual_in) || !aligned16(residual_out) ||
@@ -136,7 +145,8 @@ rq_status dynamic_tensor_call(const void *x, const void *residual_in, void *resi
         const Span ins[] = {span(x, tb), span(residual_in, tb), span(weight, hidden * 2)};
         const Span outs[] = {span(residual_out, tb), span(norm_out, tb),
                              span(q, nvfp4 ? rows * hidden / 2 : rows * hidden),
-                             span(nvfp4 ? sf : nullptr, rows * hidden / 16), span(d_scale_out, 4)};
+                             span(nvfp4 ? sf : nullptr, sf_bytes(rows, hidden, sf_swizzled)),
+                             span(d_scale_out, 4)};
         if (bad_alias(outs, 5, ins, 3, 0, 1)) return RQ_ERR_ALIAS;
     }
     st = cuda_status(cudaMemsetAsync(d_scale_out, 0, sizeof(float), s));
@@ -152,6 +162,32 @@ rq_status dynamic_tensor_call(const void *x, const void *residual_in, void *resi
     auto p = make_params(x, residual_in, residual_out, weight, eps, d_scale_out, q, sf, norm_out,
                          nullptr, rows, hidden);
     return launch_rows<MODE>(p, dt, stream);
+}
+
+rq_status nvfp4_call(const void *x, const void *residual_in, void *residual_out, const void *weight,
+                     float eps, const float *d_global_scale, uint8_t *q_packed,
+                     uint8_t *block_scales, void *norm_out, int64_t rows, int64_t hidden,
+                     rq_dtype dt, rq_stream_t stream, int sf_swizzled)
+{
+    rq_status st = check_rows(rows, hidden, dt);
+    if (st != RQ_OK || rows == 0) return st;
+    if (!x || !residual_in || !residual_out || !weight || !d_global_scale || !q_packed ||
+        !block_scales)
+        return RQ_ERR_NULL;
+    if (!aligned16(x) || !aligned16(residual_in) || !aligned16(residual_out) || !aligned16(weight) ||
+        !aligned16(q_packed) || !aligned16(block_scales) || (norm_out && !aligned16(norm_out)) ||
+        !aligned4(d_global_scale))
+        return RQ_ERR_MISALIGNED;
+    const int64_t tb = rows * hidden * 2;
+    const Span ins[] = {span(x, tb), span(residual_in, tb), span(weight, hidden * 2),
+                        span(d_global_scale, 4)};
+    const Span outs[] = {span(residual_out, tb), span(norm_out, tb), span(q_packed, rows * hidden / 2),
+                         span(block_scales, sf_bytes(rows, hidden, sf_swizzled))};
+    if (bad_alias(outs, 4, ins, 4, 0, 1)) return RQ_ERR_ALIAS;
+    auto p = make_params(x, residual_in, residual_out, weight, eps, d_global_scale, q_packed,
+                         block_scales, norm_out, nullptr, rows, hidden);
+    return sf_swizzled ? launch_rows<rq::MODE_NVFP4_SWZ>(p, dt, stream)
+                       : launch_rows<rq::MODE_NVFP4>(p, dt, stream);
 }
 
 }  // namespace
@@ -183,24 +219,18 @@ rq_status rq_add_rmsnorm_nvfp4(const void *x, const void *residual_in, void *res
                                uint8_t *q_packed, uint8_t *block_scales, void *norm_out,
                                int64_t rows, int64_t hidden, rq_dtype dt, rq_stream_t stream)
 {
-    rq_status st = check_rows(rows, hidden, dt);
-    if (st != RQ_OK || rows == 0) return st;
-    if (!x || !residual_in || !residual_out || !weight || !d_global_scale || !q_packed ||
-        !block_scales)
-        return RQ_ERR_NULL;
-    if (!aligned16(x) || !aligned16(residual_in) || !aligned16(residual_out) || !aligned16(weight) ||
-        !aligned16(q_packed) || !aligned16(block_scales) || (norm_out && !aligned16(norm_out)) ||
-        !aligned4(d_global_scale))
-        return RQ_ERR_MISALIGNED;
-    const int64_t tb = rows * hidden * 2;
-    const Span ins[] = {span(x, tb), span(residual_in, tb), span(weight, hidden * 2),
-                        span(d_global_scale, 4)};
-    const Span outs[] = {span(residual_out, tb), span(norm_out, tb), span(q_packed, rows * hidden / 2),
-                         span(block_scales, rows * hidden / 16)};
-    if (bad_alias(outs, 4, ins, 4, 0, 1)) return RQ_ERR_ALIAS;
-    auto p = make_params(x, residual_in, residual_out, weight, eps, d_global_scale, q_packed,
-                         block_scales, norm_out, nullptr, rows, hidden);
-    return launch_rows<rq::MODE_NVFP4>(p, dt, stream);
+    return nvfp4_call(x, residual_in, residual_out, weight, eps, d_global_scale, q_packed,
+                      block_scales, norm_out, rows, hidden, dt, stream, 0);
+}
+
+rq_status rq_add_rmsnorm_nvfp4_swizzled(const void *x, const void *residual_in, void *residual_out,
+                                        const void *weight, float eps, const float *d_global_scale,
+                                        uint8_t *q_packed, uint8_t *block_scales, void *norm_out,
+                                        int64_t rows, int64_t hidden, rq_dtype dt,
+                                        rq_stream_t stream)
+{
+    return nvfp4_call(x, residual_in, residual_out, weight, eps, d_global_scale, q_packed,
+                      block_scales, norm_out, rows, hidden, dt, stream, 1);
 }
 
 rq_status rq_add_rmsnorm_amax(const void *x, const void *residual_in, const void *weight, float eps,
@@ -282,6 +312,18 @@ rq_status rq_add_rmsnorm_nvfp4_dynamic(const void *x, const void *residual_in, v
                                        rq_stream_t stream)
 {
     return dynamic_tensor_call<rq::MODE_NVFP4>(x, residual_in, residual_out, weight, eps,
+                                               d_global_scale_out, q_packed, block_scales, norm_out,
+                                               rows, hidden, dt, stream);
+}
+
+rq_status rq_add_rmsnorm_nvfp4_dynamic_swizzled(const void *x, const void *residual_in,
+                                                void *residual_out, const void *weight, float eps,
+                                                float *d_global_scale_out, uint8_t *q_packed,
+                                                uint8_t *block_scales, void *norm_out,
+                                                int64_t rows, int64_t hidden, rq_dtype dt,
+                                                rq_stream_t stream)
+{
+    return dynamic_tensor_call<rq::MODE_NVFP4_SWZ>(x, residual_in, residual_out, weight, eps,
                                                d_global_scale_out, q_packed, block_scales, norm_out,
                                                rows, hidden, dt, stream);
 }
@@ -395,7 +437,12 @@ size_t rq_nvfp4_packed_bytes(int64_t rows, int64_t hidden)
 
 size_t rq_nvfp4_scale_bytes(int64_t rows, int64_t hidden)
 {
-    return rows > 0 && hidden > 0 ? (size_t)rows * (size_t)(hidden / 16) : 0;
+    return rows > 0 && hidden > 0 ? (size_t)sf_bytes(rows, hidden, 0) : 0;
+}
+
+size_t rq_nvfp4_swizzled_scale_bytes(int64_t rows, int64_t hidden)
+{
+    return rows > 0 && hidden > 0 ? (size_t)sf_bytes(rows, hidden, 1) : 0;
 }
 
 const char *rq_status_string(rq_status status)
@@ -415,6 +462,6 @@ const char *rq_status_string(rq_status status)
 
 const char *rq_last_error(void) { return g_last_error; }
 
-int rq_version(void) { return 100; }
+int rq_version(void) { return 200; }
 
 }  // extern "C"

@@ -17,7 +17,7 @@ struct NormQuantParams {
     const void *w;
     void *norm_out;      // may be null
     uint8_t *q;          // FP8 codes [rows, H] or NVFP4 packed [rows, H/2]
-    uint8_t *sf;         // NVFP4 block scales [rows, H/16]
+    uint8_t *sf;         // NVFP4 block scales (layout below)
     const float *scale;  // FP8 dequant scale or NVFP4 global scale
     float *amax;         // amax-mode output
     float *row_scales;   // per-row FP8 scales [rows] (per-token mode)
@@ -25,6 +25,8 @@ struct NormQuantParams {
     int64_t rows;
     int hidden;
     int nvec;            // hidden / 8
+    int sf_col_tiles;    // swizzled scales: tiles of 4 block columns per row of tiles,
+                         // ceil(H / 64)
 };
 
 struct QKParams {
@@ -48,7 +50,12 @@ struct QKParams {
     int64_t num_slots;       // rows of the K pool
 };
 
-enum QuantMode { MODE_FP8 = 0, MODE_NVFP4 = 1, MODE_AMAX = 2, MODE_FP8_ROW = 3 };
+// MODE_NVFP4 writes the block scales row-major [rows, H/16]; MODE_NVFP4_SWZ
+// writes them in the 128 x 4-tile layout of block-scaled GEMMs (sf_offset).
+enum QuantMode { MODE_FP8 = 0, MODE_NVFP4 = 1, MODE_AMAX = 2, MODE_FP8_ROW = 3, MODE_NVFP4_SWZ = 4 };
+
+template <int MODE>
+__host__ __device__ constexpr bool is_nvfp4() { return MODE == MODE_NVFP4 || MODE == MODE_NVFP4_SWZ; }
 
 // SM count of device `dev` (cached).
 int device_sms(int dev);

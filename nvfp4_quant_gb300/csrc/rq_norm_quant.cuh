@@ -36,6 +36,63 @@ struct GroupShape {
     static constexpr int kWarpsPerGroup = G > 32 ? G / 32 : 1;
 };
 
+// Byte offset of the block scale of (row, block column c).  Linear layout:
+// row-major [rows, H/16].  Swizzled layout (the one a block-scaled NVFP4 GEMM
+// reads): the scale matrix, padded to 128-row and 4-column multiples, is cut
+// into 128 x 4 tiles of 512 bytes, the row of tiles outermost; inside a tile
+// (r, c) sits at 16 * (r % 32) + 4 * (r / 32) + c.  In both, the four scales
+// of block columns 4j..4j+3 of a row are four consecutive bytes.
+template <bool kSwz>
+__device__ __forceinline__ int64_t sf_offset(const NormQuantParams &p, int64_t row, int c)
+{
+    if (!kSwz) return row * (p.hidden / 16) + c;
+    return ((row >> 7) * p.sf_col_tiles + (c >> 2)) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4 +
+           (c & 3);
+}
+
+// Swizzled layout: zero bytes for the rows that pad the last row of tiles,
+// one 32-bit word per (row, column tile), spread over the whole grid.  (The
+// padding columns of real rows are written by the thread that stores the
+// row's last block scale.)
+__device__ __forceinline__ void sf_zero_pad_rows(const NormQuantParams &p)
+{
+    const int64_t first = p.rows;
+    const int64_t words = ((first + 127) / 128 * 128 - first) * p.sf_col_tiles;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < words;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = first + i / p.sf_col_tiles;
+        const int ct = (int)(i % p.sf_col_tiles);
+        st4(p.sf + sf_offset<true>(p, r, ct * 4), 0u);
+    }
+}
+
+// Stores the block scale sfc of block column c = k / 2 (k = this lane's
+// vector index; the lanes of vectors k and k + 1 hold the same scale).  With
+// whole groups of four columns (hidden % 64 == 0) the lane of k % 8 == 0
+// stores the four scales of its group as one word, gathered from the lanes
+// 2, 4 and 6 above it; otherwise each even-k lane stores its byte, and in the
+// swizzled layout the lane of the last column also zeroes the padding
+// columns after it.  Every lane of the warp must call this (shuffles).
+template <bool kSwz>
+__device__ __forceinline__ void store_block_scale(const NormQuantParams &p, int64_t row, int k,
+                                                  bool ok, uint32_t sfc, bool sf_words)
+{
+    // linear layout: the row's scales start at row * H/16
+    uint8_t *base = kSwz ? p.sf : p.sf + row * (int64_t)(p.hidden / 16);
+    auto at = [&](int c) { return kSwz ? base + sf_offset<true>(p, row, c) : base + c; };
+    if (sf_words) {
+        const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, sfc, 2);
+        const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sfc, 4);
+        const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sfc, 6);
+        if (ok && (k & 7) == 0) st4(at(k / 2), sfc | (b1 << 8) | (b2 << 16) | (b3 << 24));
+    } else if (ok && (k & 1) == 0) {
+        st1(at(k / 2), sfc);
+        const int nb = p.hidden / 16;
+        if (kSwz && k / 2 == nb - 1)
+            for (int cc = nb; cc < p.sf_col_tiles * 4; ++cc) st1(at(cc), 0u);
+    }
+}
+
 // kFast: the FP8 divisor is in the range of the branch-free division (the
 // kernel picks the body once; see Divisor).
 template <typename DT, int G, int VPT, int MODE, bool kFast>
@@ -57,7 +114,7 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
         wv[j] = k < nvec ? ld_keep16(static_cast<const uint8_t *>(p.w) + (int64_t)k * 16)
                          : make_uint4(0, 0, 0, 0);
     }
-    const float scale = (MODE == MODE_FP8 || MODE == MODE_NVFP4) ? ld_f32(p.scale) : 1.0f;
+    const float scale = (MODE == MODE_FP8 || is_nvfp4<MODE>()) ? ld_f32(p.scale) : 1.0f;
     const Divisor by_scale(scale);  // FP8: y / scale
     const Divisor by_six(6.0f);     // NVFP4: (gs * amax) / 6
     const bool sf_words = (p.hidden % 64) == 0;  // 4 block scales per 32-bit store
@@ -141,7 +198,7 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
                 for (int e = 0; e < 8; ++e) v[e] = div_by<kFast>(y[e], by_scale);
                 const uint2 c = e4m3x8(v);
                 if (ok) st8(p.q + row * H + (int64_t)k * 8, c.x, c.y);
-            } else if (MODE == MODE_NVFP4) {
+            } else if (is_nvfp4<MODE>()) {
                 float m = 0.0f;
 #pragma unroll
                 for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(y[e]));
@@ -155,16 +212,7 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
                 for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(y[e], enc);
                 const uint32_t codes = e2m1x8(v);
                 if (ok) st4(p.q + row * (H / 2) + (int64_t)k * 4, codes);
-                // block scales: lane t (k even) owns block k/2
-                uint8_t *sfrow = p.sf + row * (H / 16);
-                if (sf_words) {
-                    const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, sfc, 2);
-                    const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sfc, 4);
-                    const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sfc, 6);
-                    if (ok && (k & 7) == 0) st4(sfrow + k / 2, sfc | (b1 << 8) | (b2 << 16) | (b3 << 24));
-                } else if (ok && (k & 1) == 0) {
-                    st1(sfrow + k / 2, sfc);
-                }
+                store_block_scale<MODE == MODE_NVFP4_SWZ>(p, row, k, ok, sfc, sf_words);
             } else if (MODE == MODE_FP8_ROW) {
                 sv[j] = yv;  // residual' is stored; keep the rounded y for the second pass
                 if (ok) {
@@ -214,6 +262,8 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
             }
         }
     }
+
+    if (MODE == MODE_NVFP4_SWZ) sf_zero_pad_rows(p);
 
     if (MODE == MODE_AMAX) {
         // block maximum, then one atomic per CTA on the float's bit pattern

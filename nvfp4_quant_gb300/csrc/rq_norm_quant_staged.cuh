@@ -33,7 +33,7 @@ __device__ __forceinline__ void staged_body(const NormQuantParams &p, uint4 *buf
     uint4 *rs = buf + nvec;   // residual, then residual'
     const uint8_t *w = static_cast<const uint8_t *>(p.w);
 
-    const float scale = (MODE == MODE_FP8 || MODE == MODE_NVFP4) ? ld_f32(p.scale) : 1.0f;
+    const float scale = (MODE == MODE_FP8 || is_nvfp4<MODE>()) ? ld_f32(p.scale) : 1.0f;
     const Divisor by_scale(scale);
     const Divisor by_six(6.0f);
     const bool sf_words = (p.hidden % 64) == 0;
@@ -110,7 +110,7 @@ __device__ __forceinline__ void staged_body(const NormQuantParams &p, uint4 *buf
                 for (int e = 0; e < 8; ++e) v[e] = div_by<kFast>(y[e], by_scale);
                 const uint2 c = e4m3x8(v);
                 if (ok) st8(p.q + row * H + (int64_t)k * 8, c.x, c.y);
-            } else if (MODE == MODE_NVFP4) {
+            } else if (is_nvfp4<MODE>()) {
                 float m = 0.0f;
 #pragma unroll
                 for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(y[e]));
@@ -124,15 +124,7 @@ __device__ __forceinline__ void staged_body(const NormQuantParams &p, uint4 *buf
                 for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(y[e], enc);
                 const uint32_t codes = e2m1x8(v);
                 if (ok) st4(p.q + row * (H / 2) + (int64_t)k * 4, codes);
-                uint8_t *sfrow = p.sf + row * (H / 16);
-                if (sf_words) {
-                    const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, sfc, 2);
-                    const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sfc, 4);
-                    const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sfc, 6);
-                    if (ok && (k & 7) == 0) st4(sfrow + k / 2, sfc | (b1 << 8) | (b2 << 16) | (b3 << 24));
-                } else if (ok && (k & 1) == 0) {
-                    st1(sfrow + k / 2, sfc);
-                }
+                store_block_scale<MODE == MODE_NVFP4_SWZ>(p, row, k, ok, sfc, sf_words);
             } else if (MODE == MODE_FP8_ROW) {
                 if (ok) {
                     sts16(xs + k, yv);  // the rounded y, for the pass after the row maximum
@@ -179,6 +171,8 @@ __device__ __forceinline__ void staged_body(const NormQuantParams &p, uint4 *buf
 
     cp_async_commit();
     cp_async_wait<0>();  // nothing may stay in flight at exit
+
+    if (MODE == MODE_NVFP4_SWZ) sf_zero_pad_rows(p);
 
     if (MODE == MODE_AMAX) {
         float m = group_max<32>(amax_acc);

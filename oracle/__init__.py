@@ -50,6 +50,8 @@ def lib():
             "oracle_add_rmsnorm_nvfp4": (None, [i32, u16p, u16p, u16p, f32, f32, i64, i64,
                                                 u16p, u16p, u8p, u8p]),
             "oracle_amax": (ctypes.c_float, [i32, u16p, i64]),
+            "oracle_nvfp4_swizzled_scale_bytes": (i64, [i64, i64]),
+            "oracle_nvfp4_swizzle_scales": (None, [u8p, i64, i64, u8p]),
             "oracle_fp8_scale_from_amax": (ctypes.c_float, [f32]),
             "oracle_fp8_dynamic_scale": (ctypes.c_float, [f32]),
             "oracle_nvfp4_dynamic_gs": (ctypes.c_float, [f32]),
@@ -240,6 +242,21 @@ def qk_rmsnorm_rope_fp8(dt, src, token_stride, n_tokens, n_heads, head_dim, w, e
                                      max_pos, scale, _p(o, ctypes.c_uint16),
                                      _p(q, ctypes.c_uint8))
     return o, q
+
+
+def nvfp4_swizzled_scale_bytes(rows, hidden):
+    return int(lib().oracle_nvfp4_swizzled_scale_bytes(rows, hidden))
+
+
+def nvfp4_swizzle_scales(sf, hidden):
+    """Linear [rows, hidden/16] block scales -> the 128 x 4-tile GEMM layout
+    (1-D uint8, padding bytes 0)."""
+    sf = np.ascontiguousarray(sf, np.uint8)
+    rows = sf.shape[0]
+    assert sf.shape == (rows, hidden // 16)
+    out = np.empty(nvfp4_swizzled_scale_bytes(rows, hidden), np.uint8)
+    lib().oracle_nvfp4_swizzle_scales(_p(sf, ctypes.c_uint8), rows, hidden, _p(out, ctypes.c_uint8))
+    return out
 
 
 def nvfp4_dequant(packed, sf, gs):

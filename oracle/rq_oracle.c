@@ -268,6 +268,31 @@ void oracle_add_rmsnorm_nvfp4(int dt, const uint16_t *x, const uint16_t *r,
     oracle_quant_nvfp4(dt, y_out, rows, hidden, gs, packed, sf);
 }
 
+int64_t oracle_nvfp4_swizzled_scale_bytes(int64_t rows, int64_t hidden)
+{
+    int64_t nb = hidden / 16;
+    int64_t rows_pad = (rows + 127) / 128 * 128;
+    int64_t cols_pad = (nb + 3) / 4 * 4;
+    return rows_pad * cols_pad;
+}
+
+void oracle_nvfp4_swizzle_scales(const uint8_t *sf, int64_t rows,
+                                 int64_t hidden, uint8_t *out)
+{
+    int64_t nb = hidden / 16;
+    int64_t rows_pad = (rows + 127) / 128 * 128;
+    int64_t cols_pad = (nb + 3) / 4 * 4;
+    int64_t tiles_per_row = cols_pad / 4;
+    for (int64_t r = 0; r < rows_pad; ++r) {
+        for (int64_t c = 0; c < cols_pad; ++c) {
+            uint8_t v = (r < rows && c < nb) ? sf[r * nb + c] : 0;
+            int64_t tile = (r / 128) * tiles_per_row + c / 4;
+            int64_t rr = r % 128, cc = c % 4;
+            out[tile * 512 + 16 * (rr % 32) + 4 * (rr / 32) + cc] = v;
+        }
+    }
+}
+
 float oracle_amax(int dt, const uint16_t *v, int64_t n)
 {
     float a = 0.0f;

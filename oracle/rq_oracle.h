@@ -97,6 +97,24 @@ void oracle_add_rmsnorm_nvfp4(int dt, const uint16_t *x, const uint16_t *r,
                               int64_t rows, int64_t hidden, uint16_t *s_out,
                               uint16_t *y_out, uint8_t *packed, uint8_t *sf);
 
+/* GEMM-facing block-scale layout.  The pages size the block-scale tensor for
+ * the GEMM that consumes it ("Add AutoDeploy NVFP4 RMSNorm quant fusion",
+ * review: the sf_size math of the shape-only ops; "[Performance]: Fuse local
+ * NVFP4 tail after NCCL fallback", Correctness: the expected packed NVFP4
+ * output shape) but do not print the layout.  The one written here is the
+ * layout the block-scaled NVFP4 GEMM of cuBLASLt (16-element blocks, E4M3
+ * scales) reads for an operand: the rows x nb scale matrix (nb = hidden/16)
+ * is padded with zero bytes to a multiple of 128 rows and of 4 block
+ * columns and cut into 128 x 4 tiles of 512 bytes, stored with the row of
+ * tiles outermost; inside a tile the scale of (row r, block column c) is
+ * byte 16*(r mod 32) + 4*(r div 32) + c.  Pinned by feeding its output to
+ * that GEMM (GPU test), not by the pages.
+ *   sf:  [rows, hidden/16] linear scales (as oracle_quant_nvfp4 writes them)
+ *   out: oracle_nvfp4_swizzled_scale_bytes(rows, hidden) bytes, all written */
+int64_t oracle_nvfp4_swizzled_scale_bytes(int64_t rows, int64_t hidden);
+void oracle_nvfp4_swizzle_scales(const uint8_t *sf, int64_t rows,
+                                 int64_t hidden, uint8_t *out);
+
 /* Dynamic scales.  A scale derived from an absolute maximum of zero (an
  * all-zero row or tensor) is taken as 1, so that every code is a signed zero
  * and the dequantised values are zero, instead of the 0/0 of the plain

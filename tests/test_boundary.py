@@ -64,6 +64,15 @@ def nvfp4(L, **kw):
                                   a["y"], a["rows"], a["hidden"], a["dt"], None)
 
 
+def nvfp4_swz(L, **kw):
+    a = dict(x=A["x"], r=A["r"], ro=A["ro"], w=A["w"], eps=1e-6, s=A["s"], q=A["q"], sf=A["sf"],
+             y=A["y"], rows=16, hidden=128, dt=1)
+    a.update(kw)
+    return L.rq_add_rmsnorm_nvfp4_swizzled(a["x"], a["r"], a["ro"], a["w"], a["eps"], a["s"],
+                                           a["q"], a["sf"], a["y"], a["rows"], a["hidden"],
+                                           a["dt"], None)
+
+
 def qk(L, **kw):
     a = dict(q=A["x"], k=A["k"], qst=16 * 128, kst=8 * 128, T=32, hq=16, hk=8, hd=128, qw=A["w"],
              kw=A["r"], eps=1e-6, pos=A["pos"], cs=A["cs"], maxp=4096, qs=A["qs"], ks=A["ks"],
@@ -74,7 +83,7 @@ def qk(L, **kw):
                                     a["maxp"], a["qs"], a["ks"], a["qo"], a["ko"], a["dt"], None)
 
 
-@pytest.mark.parametrize("call", [fp8, nvfp4])
+@pytest.mark.parametrize("call", [fp8, nvfp4, nvfp4_swz])
 def test_row_call_rejections(L, call):
     assert call(L, rows=0) == OK  # nothing to do, no launch
     assert call(L, rows=0, x=None, r=None, ro=None, q=None) == OK  # empty tensors, null data
@@ -107,6 +116,21 @@ def test_nvfp4_specific_rejections(L):
     assert nvfp4(L, sf=A["sf"] + 1) == MISAL
     assert nvfp4(L, sf=A["q"] + 16 * 64 - 16) == ALIAS  # scales inside the packed codes
     assert nvfp4(L, y=None, rows=0) == OK  # norm output is optional
+
+
+def test_swizzled_scale_size_and_rejections(L):
+    # padded to 128-row and 4-block-column multiples
+    assert rq.rq_nvfp4_swizzled_scale_bytes(16, 128) == 128 * 8
+    assert rq.rq_nvfp4_swizzled_scale_bytes(130, 96) == 256 * 8
+    assert rq.rq_nvfp4_swizzled_scale_bytes(128, 64) == 128 * 4
+    assert rq.rq_nvfp4_swizzled_scale_bytes(16384, 7168) == 16384 * 448
+    assert rq.rq_nvfp4_swizzled_scale_bytes(0, 7168) == 0
+    assert nvfp4_swz(L, sf=None) == NULL
+    assert nvfp4_swz(L, sf=A["sf"] + 4) == MISAL
+    # 16 rows take a whole 128-row tile (1024 bytes here): a scale buffer
+    # ending 512 bytes before the packed codes in linear terms overlaps them
+    assert nvfp4_swz(L, sf=A["q"] - 512) == ALIAS
+    assert nvfp4_swz(L, y=None, rows=0) == OK
 
 
 def test_amax_rejections(L):
@@ -171,6 +195,12 @@ def test_dynamic_rejections(L):
     assert nv(sf=None) == NULL
     assert nv(sf=A["sf"] + 4) == MISAL
     assert nv(gs=A["sf"]) == ALIAS
+    nvs = lambda **kw: L.rq_add_rmsnorm_nvfp4_dynamic_swizzled(
+        A["x"], A["r"], A["ro"], A["w"], 1e-6, kw.get("gs", A["s"]), A["q"], kw.get("sf", A["sf"]),
+        None, 16, 128, 1, None)
+    assert nvs(sf=None) == NULL
+    assert nvs(sf=A["sf"] + 4) == MISAL
+    assert nvs(gs=A["sf"] + 512) == ALIAS  # inside the padded 1024-byte scale buffer
 
 
 def test_kv_store_rejections(L):
