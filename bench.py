@@ -343,12 +343,16 @@ def run_ours(args):
 def measure_next_rows(wl, peak_kind_gbs, iters=50):
     """Calls beyond the step, timed on their own: per-token FP8 on the prefill
     workload, per-tensor dynamic FP8 / NVFP4 (amax pass + fused pass) on the
-    prefill / large NVFP4 workloads, and the Q/K call storing K into a KV pool
-    of 8192 slots at shuffled slot indices."""
+    prefill / large NVFP4 workloads, the large NVFP4 call with its block
+    scales in the swizzled GEMM layout (same bytes: 16,384 rows and 7168
+    columns need no padding), and the Q/K call storing K into a KV pool of
+    8192 slots at shuffled slot indices."""
     rq, d = wl.rq, wl.d
     f = lambda: torch.zeros(1, dtype=torch.float32, device="cuda")
     row_scales = torch.empty(FP8_ROWS, dtype=torch.float32, device="cuda")
     s3, g5 = f(), f()
+    sf_swz = torch.empty(rq.rq_nvfp4_swizzled_scale_bytes(NV_ROWS, NV_H), dtype=torch.uint8,
+                         device="cuda")
     cases = [
         ("add_rmsnorm_fp8_per_token", FP8_ROWS,
          FP8_ROWS * FP8_H * 7 + FP8_ROWS * 4 + FP8_H * 2,
@@ -361,6 +365,9 @@ def measure_next_rows(wl, peak_kind_gbs, iters=50):
          alg_bytes_nvfp4(NV_ROWS, NV_H) + NV_ROWS * NV_H * 4 + NV_H * 2 + 4,
          lambda: rq.rq_add_rmsnorm_nvfp4_dynamic(d["x5"], d["r5"], wl.ro5, wl.w5, EPS, g5, wl.p5,
                                                  wl.sf5, wl.y5)),
+        ("add_rmsnorm_nvfp4_swizzled", NV_ROWS, alg_bytes_nvfp4(NV_ROWS, NV_H),
+         lambda: rq.rq_add_rmsnorm_nvfp4_swizzled(d["x5"], d["r5"], wl.ro5, wl.w5, EPS, wl.gs5,
+                                                  wl.p5, sf_swz, wl.y5)),
     ]
     n_slots = 2 * QK_T
     pool = torch.empty((n_slots, QK_HK, QK_D), dtype=torch.uint8, device="cuda")

@@ -73,18 +73,29 @@ __device__ __forceinline__ void sf_zero_pad_rows(const NormQuantParams &p)
 // 2, 4 and 6 above it; otherwise each even-k lane stores its byte, and in the
 // swizzled layout the lane of the last column also zeroes the padding
 // columns after it.  Every lane of the warp must call this (shuffles).
+// Swizzled layout: where the row's bytes of its first tile start (the row's
+// part of sf_offset); block column c adds (c / 4) * 512 + c % 4.  (Computing
+// it once per row at the top of the row loop, instead of at each store, made
+// the 16,384 x 7168 call 11 % slower: the loads of the row issue later.)
+__device__ __forceinline__ uint8_t *sf_swizzled_row(const NormQuantParams &p, int64_t row)
+{
+    return p.sf + (((row >> 7) * p.sf_col_tiles) << 9) + ((row & 31) << 4) + (((row >> 5) & 3) << 2);
+}
+
 template <bool kSwz>
 __device__ __forceinline__ void store_block_scale(const NormQuantParams &p, int64_t row, int k,
                                                   bool ok, uint32_t sfc, bool sf_words)
 {
-    // linear layout: the row's scales start at row * H/16
-    uint8_t *base = kSwz ? p.sf : p.sf + row * (int64_t)(p.hidden / 16);
-    auto at = [&](int c) { return kSwz ? base + sf_offset<true>(p, row, c) : base + c; };
+    // linear: the row's scales start at row * H/16
+    uint8_t *base = kSwz ? sf_swizzled_row(p, row) : p.sf + row * (int64_t)(p.hidden / 16);
+    auto at = [&](int c) { return kSwz ? base + ((c >> 2) << 9) + (c & 3) : base + c; };
     if (sf_words) {
         const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, sfc, 2);
         const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sfc, 4);
         const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sfc, 6);
-        if (ok && (k & 7) == 0) st4(at(k / 2), sfc | (b1 << 8) | (b2 << 16) | (b3 << 24));
+        // a word starts at a column multiple of 4: k % 8 == 0, c = k / 2
+        uint8_t *dst = kSwz ? base + ((k >> 3) << 9) : base + k / 2;
+        if (ok && (k & 7) == 0) st4(dst, sfc | (b1 << 8) | (b2 << 16) | (b3 << 24));
     } else if (ok && (k & 1) == 0) {
         st1(at(k / 2), sfc);
         const int nb = p.hidden / 16;
