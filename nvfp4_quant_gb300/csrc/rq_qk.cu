@@ -16,9 +16,12 @@
 // each lane loads its 8 cos and 8 sin values once per unit and keeps them in
 // registers for all its heads.  The kPairs head loads of a unit are issued
 // before any of them is used, so each lane has kPairs 16-byte loads in
-// flight; units of a few heads keep the tail of the grid short.  The sum of squares is a
-// 16-lane shuffle tree; the rounded normalised values are exchanged with one
-// 4-word shuffle.
+// flight; units of a few heads keep the tail of the grid short.  Element
+// pairs go through Blackwell's packed fp32 multiply / add / FMA (each half an
+// IEEE round-to-nearest operation, so the results are the scalar ones): the
+// sum of squares is two interleaved partial sums per lane, then a 16-lane
+// shuffle tree; the rounded normalised values are exchanged with one 4-word
+// shuffle.
 #include "rq_device.cuh"
 #include "rq_launch.h"
 
@@ -58,16 +61,17 @@ __device__ __forceinline__ void qk_body(const QKParams &p)
         const uint8_t *cs = reinterpret_cast<const uint8_t *>(p.cos_sin + (int64_t)pos * kHeadDim);
         const uint4 c0 = ld_keep16(cs + rot * 4), c1 = ld_keep16(cs + rot * 4 + 16);
         const uint4 s0 = ld_keep16(cs + (64 + rot) * 4), s1 = ld_keep16(cs + (64 + rot) * 4 + 16);
-        const float c[8] = {__uint_as_float(c0.x), __uint_as_float(c0.y), __uint_as_float(c0.z),
-                            __uint_as_float(c0.w), __uint_as_float(c1.x), __uint_as_float(c1.y),
-                            __uint_as_float(c1.z), __uint_as_float(c1.w)};
+        const float2 cp[4] = {make_float2(__uint_as_float(c0.x), __uint_as_float(c0.y)),
+                              make_float2(__uint_as_float(c0.z), __uint_as_float(c0.w)),
+                              make_float2(__uint_as_float(c1.x), __uint_as_float(c1.y)),
+                              make_float2(__uint_as_float(c1.z), __uint_as_float(c1.w))};
         // lanes holding elements 0..63 subtract m * sin, the others add it:
         // fold that sign into the sine once per unit (RN(-x) = -RN(x))
         const uint32_t neg = upper ? 0u : 0x80000000u;
-        const float s[8] = {__uint_as_float(s0.x ^ neg), __uint_as_float(s0.y ^ neg),
-                            __uint_as_float(s0.z ^ neg), __uint_as_float(s0.w ^ neg),
-                            __uint_as_float(s1.x ^ neg), __uint_as_float(s1.y ^ neg),
-                            __uint_as_float(s1.z ^ neg), __uint_as_float(s1.w ^ neg)};
+        const float2 sp[4] = {make_float2(__uint_as_float(s0.x ^ neg), __uint_as_float(s0.y ^ neg)),
+                              make_float2(__uint_as_float(s0.z ^ neg), __uint_as_float(s0.w ^ neg)),
+                              make_float2(__uint_as_float(s1.x ^ neg), __uint_as_float(s1.y ^ neg)),
+                              make_float2(__uint_as_float(s1.z ^ neg), __uint_as_float(s1.w ^ neg))};
         const uint8_t *qtok = static_cast<const uint8_t *>(p.q) + tok * p.q_stride * 2;
         const uint8_t *ktok = static_cast<const uint8_t *>(p.k) + tok * p.k_stride * 2;
         // K destination row: the token itself, or its slot in the KV pool
@@ -92,22 +96,33 @@ __device__ __forceinline__ void qk_body(const QKParams &p)
             for (int u = 0; u < kPairs; ++u) {
                 const int h = h0 + 2 * u + half;
                 const bool is_q = h < p.hq;
-                // RMSNorm over the 16 lanes of the head row
+                // RMSNorm over the 16 lanes of the head row.  Element pairs
+                // (2i, 2i+1) go through Blackwell's packed fp32 ops: each half
+                // is the same IEEE operation as the scalar one.
                 float x[8];
                 unpack8<DT>(xv[u], x);
-                float ss = 0.0f;
+                float2 sq = make_float2(0.0f, 0.0f);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) ss = __fmaf_rn(x[e], x[e], ss);  // squares are exact
-                ss = group_sum<16>(ss);
+                for (int i = 0; i < 4; ++i) {
+                    const float2 xi = make_float2(x[2 * i], x[2 * i + 1]);
+                    sq = __ffma2_rn(xi, xi, sq);  // squares are exact
+                }
+                const float ss = group_sum<16>(__fadd_rn(sq.x, sq.y));
                 // ss / 128 is an exact power-of-two scaling, as the division would
                 // be; 1 / sqrt(.) as the correctly rounded reciprocal of the
                 // correctly rounded root
                 const float rstd =
                     rcp_rn(__fsqrt_rn(__fadd_rn(__fmul_rn(ss, 1.0f / kHeadDim), p.eps)));
+                const float2 r2 = make_float2(rstd, rstd);
                 float w[8], n[8], m[8];
                 unpack8<DT>(is_q ? qw : kw, w);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) n[e] = __fmul_rn(__fmul_rn(x[e], rstd), w[e]);
+                for (int i = 0; i < 4; ++i) {
+                    const float2 ni = __fmul2_rn(__fmul2_rn(make_float2(x[2 * i], x[2 * i + 1]), r2),
+                                                 make_float2(w[2 * i], w[2 * i + 1]));
+                    n[2 * i] = ni.x;
+                    n[2 * i + 1] = ni.y;
+                }
                 const uint4 nv = pack8<DT>(n);
                 // the partner half of each rotation pair
                 uint4 pv;
@@ -119,12 +134,22 @@ __device__ __forceinline__ void qk_body(const QKParams &p)
                 unpack8<DT>(pv, m);
                 float o[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = __fadd_rn(__fmul_rn(n[e], c[e]), __fmul_rn(m[e], s[e]));
+                for (int i = 0; i < 4; ++i) {
+                    const float2 oi =
+                        __fadd2_rn(__fmul2_rn(make_float2(n[2 * i], n[2 * i + 1]), cp[i]),
+                                   __fmul2_rn(make_float2(m[2 * i], m[2 * i + 1]), sp[i]));
+                    o[2 * i] = oi.x;
+                    o[2 * i + 1] = oi.y;
+                }
                 unpack8<DT>(pack8<DT>(o), o);  // FP8 from the dtype-rounded rotation
                 const Divisor &by = is_q ? by_q : by_k;
                 float v[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = div_by<kFast>(o[e], by);
+                for (int i = 0; i < 4; ++i) {
+                    const float2 vi = div_by2<kFast>(make_float2(o[2 * i], o[2 * i + 1]), by);
+                    v[2 * i] = vi.x;
+                    v[2 * i + 1] = vi.y;
+                }
                 const uint2 code = e4m3x8(v);
                 if (h < heads && (is_q || krow >= 0)) {
                     uint8_t *dst = is_q ? p.q_out + (tok * p.hq + h) * kHeadDim

@@ -2,15 +2,17 @@
 // Markstein's correction step) with CUDA's correctly rounded __fdiv_rn over
 // every finite fp32 dividend, for each divisor given on the command line.
 // Prints, per divisor: the fp32 quotients that differ where the reference
-// quotient has magnitude in [2^-40, 2^20), and the E4M3 codes (satfinite)
-// that differ anywhere, NaN and infinite dividends included.  Built and run by tests/test_gpu_division.py.
+// quotient has magnitude in [2^-40, 2^20), the E4M3 codes (satfinite)
+// that differ anywhere, NaN and infinite dividends included, and the results
+// of the packed two-wide version (rq::div_by2, on the pair (a, -a)) that are
+// not bit for bit the scalar version's.  Built and run by tests/test_gpu_division.py.
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
 
 #include "rq_device.cuh"
 
-__device__ unsigned long long g_quot_diff, g_code_diff;
+__device__ unsigned long long g_quot_diff, g_code_diff, g_pack_diff;
 __device__ unsigned int g_first_bad;
 
 __global__ void check(float b)
@@ -29,6 +31,12 @@ __global__ void check(float b)
         }
         if ((rq::e4m3x2(ref, 0.0f) & 0xFF) != (rq::e4m3x2(got, 0.0f) & 0xFF))
             atomicAdd(&g_code_diff, 1ull);
+        const float na = __uint_as_float(bits ^ 0x80000000u);
+        const float got_n = d.fast ? rq::div_by<true>(na, d) : rq::div_by<false>(na, d);
+        const float2 g2 = d.fast ? rq::div_by2<true>(make_float2(a, na), d)
+                                 : rq::div_by2<false>(make_float2(a, na), d);
+        if (__float_as_uint(g2.x) != __float_as_uint(got) || __float_as_uint(g2.y) != __float_as_uint(got_n))
+            atomicAdd(&g_pack_diff, 1ull);
     }
 }
 
@@ -42,6 +50,7 @@ int main(int argc, char **argv)
         unsigned int z = 0;
         cudaMemcpyToSymbol(g_quot_diff, &zero, sizeof(zero));
         cudaMemcpyToSymbol(g_code_diff, &zero, sizeof(zero));
+        cudaMemcpyToSymbol(g_pack_diff, &zero, sizeof(zero));
         cudaMemcpyToSymbol(g_first_bad, &z, sizeof(z));
         check<<<sms * 8, 256>>>(b);
         cudaError_t e = cudaDeviceSynchronize();
@@ -49,12 +58,14 @@ int main(int argc, char **argv)
             std::printf("error %s\n", cudaGetErrorString(e));
             return 2;
         }
-        unsigned long long qd = 0, cd = 0;
+        unsigned long long qd = 0, cd = 0, pd = 0;
         unsigned int first = 0;
         cudaMemcpyFromSymbol(&qd, g_quot_diff, sizeof(qd));
         cudaMemcpyFromSymbol(&cd, g_code_diff, sizeof(cd));
+        cudaMemcpyFromSymbol(&pd, g_pack_diff, sizeof(pd));
         cudaMemcpyFromSymbol(&first, g_first_bad, sizeof(first));
-        std::printf("divisor %.9g quotient_diffs %llu code_diffs %llu first 0x%08x\n", b, qd, cd, first);
+        std::printf("divisor %.9g quotient_diffs %llu code_diffs %llu first 0x%08x packed_diffs %llu\n", b, qd,
+                    cd, first, pd);
     }
     return 0;
 }

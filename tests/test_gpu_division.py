@@ -37,3 +37,4 @@ def test_shared_divisor_division_is_correctly_rounded(tmp_path):
     for f in lines:
         assert f[3] == "0", "quotient differs from __fdiv_rn: " + " ".join(f)
         assert f[5] == "0", "E4M3 code differs: " + " ".join(f)
+        assert f[9] == "0", "packed two-wide division differs from the scalar one: " + " ".join(f)
