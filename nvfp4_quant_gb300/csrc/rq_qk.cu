@@ -52,10 +52,14 @@ __device__ __forceinline__ void qk_body(const QKParams &p)
     const Divisor by_k(p.hk > 0 ? ld_f32(p.k_scale) : 1.0f);
 
     const int groups = (heads + 2 * kPairs - 1) / (2 * kPairs);  // units per token
-    const int64_t n_units = p.n_tokens * groups;
-    for (int64_t unit = warp0; unit < n_units; unit += nwarps) {
-        const int64_t tok = unit / groups;
-        const int h0 = (int)(unit - tok * groups) * 2 * kPairs;
+    // unit = tok * groups + g, stepped by nwarps = step_tok * groups + step_g
+    // without a 64-bit division per unit
+    const int64_t step_tok = nwarps / groups;
+    const int step_g = (int)(nwarps - step_tok * groups);
+    int64_t tok = warp0 / groups;
+    int g = (int)(warp0 - tok * groups);
+    for (; tok < p.n_tokens;) {  // unit < n_units
+        const int h0 = g * 2 * kPairs;
         int pos = ld_s32(p.pos + tok);
         pos = pos < 0 ? 0 : (pos >= p.max_pos ? (int)(p.max_pos - 1) : pos);
         const uint8_t *cs = reinterpret_cast<const uint8_t *>(p.cos_sin + (int64_t)pos * kHeadDim);
@@ -157,6 +161,12 @@ __device__ __forceinline__ void qk_body(const QKParams &p)
                     st8(dst + lane16 * 8, code.x, code.y);
                 }
             }
+        }
+        tok += step_tok;
+        g += step_g;
+        if (g >= groups) {
+            g -= groups;
+            ++tok;
         }
     }
 }
