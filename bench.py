@@ -576,20 +576,32 @@ def load_traffic(kernel):
         with open(path) as f:
             d = json.load(f)
         ent = d.get(kernel)
-        if ent and ent.get("source_hash") == source_hash():
+        if ent and ent.get("source_hash") == source_hash(kernel):
             return ent["dram_bytes_per_launch"]
     except Exception:
         pass
     return None
 
 
-def source_hash():
+# The files each profiled kernel is built from: its committed counters stand
+# only while none of them has changed.
+_ROW_SOURCES = ["include/rq.h", "nvfp4_quant_gb300/csrc/rq_api.cu", "nvfp4_quant_gb300/csrc/rq_launch.h",
+                "nvfp4_quant_gb300/csrc/rq_device.cuh", "nvfp4_quant_gb300/csrc/rq_norm_quant.cuh",
+                "nvfp4_quant_gb300/csrc/rq_norm_quant_staged.cuh",
+                "nvfp4_quant_gb300/csrc/rq_norm_quant_launch.cuh",
+                "nvfp4_quant_gb300/csrc/rq_norm_quant_bf16.cu"]
+_QK_SOURCES = ["include/rq.h", "nvfp4_quant_gb300/csrc/rq_api.cu", "nvfp4_quant_gb300/csrc/rq_launch.h",
+               "nvfp4_quant_gb300/csrc/rq_device.cuh", "nvfp4_quant_gb300/csrc/rq_qk.cu"]
+KERNEL_SOURCES = {"add_rmsnorm_nvfp4": _ROW_SOURCES, "add_rmsnorm_fp8": _ROW_SOURCES,
+                  "add_rmsnorm_nvfp4_swizzled": _ROW_SOURCES, "qk_rmsnorm_rope_fp8": _QK_SOURCES}
+
+
+def source_hash(kernel):
     import hashlib
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "nvfp4_quant_gb300", "csrc")
-    for n in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, n), "rb") as f:
-            h.update(n.encode() + f.read())
+    for rel in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(rel.encode() + f.read())
     return h.hexdigest()[:16]
 
 
