@@ -79,8 +79,9 @@ static cudaError_t launch_staged(const NormQuantParams &p, cudaStream_t stream)
     return cudaGetLastError();
 }
 
-// Thread-group shape by row length (nvec 16-byte vectors per row): the
-// smallest listed G x VPT that covers the row.  Rows above 8192 elements go
+// Thread-group shape by row length (nvec 16-byte vectors per row): with at
+// most one row per SM, a wide group (256 or 512 threads per row); otherwise
+// the smallest listed G x VPT that covers the row.  Rows above 8192 elements go
 // through shared memory while two such CTAs fit per SM (up to 28672 elements:
 // 112 KB each) and there are at least two rows per SM; measured on GB300,
 // 16384 / 16400 / 20480-element rows ran at 0.82 / 0.79 / 0.74 of the copy
@@ -90,13 +91,23 @@ template <typename DT, int MODE>
 cudaError_t launch_add_rmsnorm(const NormQuantParams &p, cudaStream_t stream)
 {
     const int n = p.nvec;
+    int dev = 0;
+    // At most one row per SM: one CTA per row either way, so give each row
+    // more threads and each thread fewer vectors (a shorter serial chain per
+    // thread; measured on GB300 in a CUDA graph, the [64, 8192] fp16 NVFP4
+    // tail with norm out went from 3.96 to 2.95 us).
+    if (n > 256 && cudaGetDevice(&dev) == cudaSuccess && p.rows <= (int64_t)device_sms(dev)) {
+        if (n <= 512) return launch_cfg<DT, 256, 2, MODE>(p, stream);
+        if (n <= 1024) return launch_cfg<DT, 512, 2, MODE>(p, stream);
+        if (n <= 2048) return launch_cfg<DT, 512, 4, MODE>(p, stream);
+        return launch_cfg<DT, 512, 8, MODE>(p, stream);
+    }
     if (n <= 16) return launch_cfg<DT, 8, 2, MODE>(p, stream);
     if (n <= 64) return launch_cfg<DT, 32, 2, MODE>(p, stream);
     if (n <= 128) return launch_cfg<DT, 32, 4, MODE>(p, stream);
     if (n <= 256) return launch_cfg<DT, 64, 4, MODE>(p, stream);
     if (n <= 512) return launch_cfg<DT, 128, 4, MODE>(p, stream);
     if (n > 1024 && n <= 3584) {
-        int dev = 0;
         if (cudaGetDevice(&dev) == cudaSuccess && p.rows >= 2 * (int64_t)device_sms(dev))
             return launch_staged<DT, MODE>(p, stream);
     }

@@ -341,3 +341,44 @@ def test_long_rows_through_shared_memory(hidden, dt):
     assert_norm_within_ulp(host16(y), y_ref, dt)
     a_ref = O.amax(dt, y_ref)
     assert abs(float(amax.item()) - a_ref) <= pins.ulp(np.array([a_ref]), dt)[0]
+
+
+# ------------------------------------------------------------- few rows
+# At most one row per SM the rows go to wide groups (256 or 512 threads per
+# row, 2 to 8 vectors per thread): every mode on each of those shapes, with
+# ragged rows (hidden not a multiple of the group's reach) and row counts 1,
+# 17 and the SM count.
+FEW_HIDDEN = [2064, 4096, 4112, 7168, 8208, 12304, 16384, 16400]
+
+
+@pytest.mark.parametrize("hidden", FEW_HIDDEN)
+@pytest.mark.parametrize("dt", ["bf16", "fp16"])
+def test_few_rows_wide_groups(hidden, dt):
+    for rows in (1, 17, SMS):
+        x, r, w = synth.rows_input(rows + hidden, rows, hidden, dt, outlier_frac=0.01)
+        gs, scale = oracle_gs(dt, x, r, w, 1e-6)
+        check_fp8(dt, x, r, w, 1e-6, scale, norm_out=True)
+        _, y, p, sf = check_nvfp4(dt, x, r, w, 1e-6, gs, norm_out=True)
+        # swizzled scales: the layout of the linear call's scales
+        tdt = torch.bfloat16 if dt == "bf16" else torch.float16
+        xd, rd, wd = dev16(x, dt), dev16(r, dt), dev16(w, dt)
+        ro = torch.empty((rows, hidden), dtype=tdt, device="cuda")
+        ps = torch.empty((rows, hidden // 2), dtype=torch.uint8, device="cuda")
+        ss = torch.full((rq.rq_nvfp4_swizzled_scale_bytes(rows, hidden),), 0xA5, dtype=torch.uint8,
+                        device="cuda")
+        rq.rq_add_rmsnorm_nvfp4_swizzled(xd, rd, ro, wd, 1e-6, f32dev(gs), ps, ss)
+        torch.cuda.synchronize()
+        assert np.array_equal(host8(ps), p)
+        assert np.array_equal(host8(ss), O.nvfp4_swizzle_scales(sf, hidden))
+        # per-token FP8: codes and scales are the oracle's quantiser of y
+        q = torch.empty((rows, hidden), dtype=torch.uint8, device="cuda")
+        sc = torch.empty((rows,), dtype=torch.float32, device="cuda")
+        rq.rq_add_rmsnorm_fp8_per_token(xd, rd, ro, wd, 1e-6, q, sc)
+        torch.cuda.synchronize()
+        q_o, sc_o = O.quant_fp8_per_row(dt, y)
+        assert np.array_equal(host8(q), q_o) and np.array_equal(sc.cpu().numpy(), sc_o)
+        # calibration: the maximum of |y|
+        am = torch.empty((1,), dtype=torch.float32, device="cuda")
+        rq.rq_add_rmsnorm_amax(xd, rd, wd, 1e-6, am)
+        torch.cuda.synchronize()
+        assert float(am.item()) == O.amax(dt, y)
