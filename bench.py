@@ -332,7 +332,11 @@ def run_ours(args):
         "clocks": clk.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        line["cpu_baseline"], inputs = cpu_baseline(args.cpu_seconds)
+        n = host_threads()
+        spent, desc = oracle_step_threads(n, inputs)
+        line["cpu_baseline_threads"] = {"value": ROWS_PER_STEP / spent, "unit": "rows/s", "cores": n,
+                                        "kind": "oracle, row-parallel", "sample": desc}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -606,16 +610,26 @@ def source_hash(kernel):
 
 
 # ------------------------------------------------------------------ CPU oracle
-def oracle_step_sample(frac_rows):
-    """Time the oracle on a sample of each call of the step; returns
-    (seconds per full step extrapolated by rows, sample description)."""
-    import oracle as O
+def oracle_inputs(frac_rows):
+    """Seeded inputs of a fraction of each call of the step (host arrays)."""
     r3 = max(1, int(FP8_ROWS * frac_rows))
     r5 = max(1, int(NV_ROWS * frac_rows))
     t4 = max(1, int(QK_T * frac_rows))
-    x3, rr3, w3 = synth.rows_input(0, r3, FP8_H, "bf16", res_std=2.0)
-    x5, rr5, w5 = synth.rows_input(0, r5, NV_H, "bf16", outlier_frac=0.01)
-    q4, k4, qw4, kw4, pos4, cs4 = synth.qk_input(0, t4, QK_HQ, QK_HK, QK_D, "bf16")
+    return {"fp8": synth.rows_input(0, r3, FP8_H, "bf16", res_std=2.0),
+            "nvfp4": synth.rows_input(0, r5, NV_H, "bf16", outlier_frac=0.01),
+            "qk": synth.qk_input(0, t4, QK_HQ, QK_HK, QK_D, "bf16")}
+
+
+def oracle_step_sample(frac_rows, inputs=None):
+    """Time the oracle on a sample of each call of the step; returns
+    (seconds per full step extrapolated by rows, seconds spent, sample
+    description, the inputs used)."""
+    import oracle as O
+    inputs = inputs or oracle_inputs(frac_rows)
+    x3, rr3, w3 = inputs["fp8"]
+    x5, rr5, w5 = inputs["nvfp4"]
+    q4, k4, qw4, kw4, pos4, cs4 = inputs["qk"]
+    r3, r5, t4 = x3.shape[0], x5.shape[0], q4.shape[0]
     O.lib()
     t = time.perf_counter()
     O.add_rmsnorm_fp8("bf16", x3, rr3, w3, EPS, 0.01)
@@ -630,16 +644,64 @@ def oracle_step_sample(frac_rows):
     full = t_fp8 * FP8_ROWS / r3 + t_qk * QK_T / t4 + t_nv * NV_ROWS / r5
     desc = ("oracle (single-threaded C) on %d of %d FP8 rows, %d of %d Q/K tokens, %d of %d "
             "NVFP4 rows; time scaled to a full step by rows" % (r3, FP8_ROWS, t4, QK_T, r5, NV_ROWS))
-    return full, t_fp8 + t_qk + t_nv, desc
+    return full, t_fp8 + t_qk + t_nv, desc, inputs
+
+
+def oracle_step_threads(n_threads, inputs=None):
+    """The same oracle, on one full step of inputs split by rows (tokens for
+    Q/K) over n_threads host threads.  The oracle is plain C called through
+    ctypes, which releases the GIL, so the slices run in parallel; nothing in
+    the oracle changes.  Returns (seconds per step, description)."""
+    import oracle as O
+    from concurrent.futures import ThreadPoolExecutor
+    if inputs is None or inputs["fp8"][0].shape[0] != FP8_ROWS or inputs["nvfp4"][0].shape[0] != NV_ROWS \
+            or inputs["qk"][0].shape[0] != QK_T:
+        inputs = oracle_inputs(1.0)
+    x3, rr3, w3 = inputs["fp8"]
+    x5, rr5, w5 = inputs["nvfp4"]
+    q4, k4, qw4, kw4, pos4, cs4 = inputs["qk"]
+    O.lib()
+
+    def cuts(n):
+        return [(i * n // n_threads, (i + 1) * n // n_threads) for i in range(n_threads)]
+
+    def fp8(a, b):
+        O.add_rmsnorm_fp8("bf16", x3[a:b], rr3[a:b], w3, EPS, 0.01)
+
+    def qk(a, b):
+        O.qk_rmsnorm_rope_fp8("bf16", q4[a:b].reshape(-1), QK_HQ * QK_D, b - a, QK_HQ, QK_D, qw4, EPS,
+                              pos4[a:b], cs4, 0.01)
+        O.qk_rmsnorm_rope_fp8("bf16", k4[a:b].reshape(-1), QK_HK * QK_D, b - a, QK_HK, QK_D, kw4, EPS,
+                              pos4[a:b], cs4, 0.01)
+
+    def nv(a, b):
+        O.add_rmsnorm_nvfp4("bf16", x5[a:b], rr5[a:b], w5, EPS, 400.0)
+
+    with ThreadPoolExecutor(max_workers=n_threads) as ex:
+        t = time.perf_counter()
+        for fn, n in ((fp8, FP8_ROWS), (qk, QK_T), (nv, NV_ROWS)):
+            list(ex.map(lambda c: fn(*c), cuts(n)))
+        spent = time.perf_counter() - t
+    desc = ("the same oracle on one full step (%d FP8 rows, %d Q/K tokens, %d NVFP4 rows), rows "
+            "split over %d host threads" % (FP8_ROWS, QK_T, NV_ROWS, n_threads))
+    return spent, desc
+
+
+def host_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
 
 
 def cpu_baseline(target_seconds):
+    """(the single-threaded baseline, the inputs it ran on)"""
     # size the sample so the oracle runs about target_seconds
-    full, spent, _ = oracle_step_sample(1.0 / 256)
+    full, spent, _, _ = oracle_step_sample(1.0 / 256)
     frac = min(1.0, (1.0 / 256) * target_seconds / max(spent, 1e-3))
-    full, spent, desc = oracle_step_sample(frac)
-    return {"value": ROWS_PER_STEP / full, "unit": "rows/s", "cores": 1, "kind": "oracle",
-            "sample": desc + " (%.1f s of CPU work)" % spent}
+    full, spent, desc, inputs = oracle_step_sample(frac)
+    return ({"value": ROWS_PER_STEP / full, "unit": "rows/s", "cores": 1, "kind": "oracle",
+             "sample": desc + " (%.1f s of CPU work)" % spent}, inputs)
 
 
 def run_reference(args):
@@ -647,11 +709,12 @@ def run_reference(args):
     if rank != 0:
         return
     frac = args.ref_fraction
+    inputs = oracle_inputs(frac)
     for _ in range(args.warmup):
-        oracle_step_sample(frac)
+        oracle_step_sample(frac, inputs)
     fulls, spents = [], []
     for _ in range(args.steps):
-        full, spent, desc = oracle_step_sample(frac)
+        full, spent, desc, _ = oracle_step_sample(frac, inputs)
         fulls.append(full)
         spents.append(spent)
     ms = statistics.mean(fulls) * 1e3
