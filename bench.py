@@ -587,14 +587,15 @@ def load_traffic(kernel):
     return None
 
 
-# The files each profiled kernel is built from: its committed counters stand
-# only while none of them has changed.
-_ROW_SOURCES = ["include/rq.h", "nvfp4_quant_gb300/csrc/rq_api.cu", "nvfp4_quant_gb300/csrc/rq_launch.h",
+# The files each profiled kernel and its launch configuration are built from
+# (not the host-side argument checks): its committed counters stand only
+# while none of them has changed.
+_ROW_SOURCES = ["include/rq.h", "nvfp4_quant_gb300/csrc/rq_launch.h",
                 "nvfp4_quant_gb300/csrc/rq_device.cuh", "nvfp4_quant_gb300/csrc/rq_norm_quant.cuh",
                 "nvfp4_quant_gb300/csrc/rq_norm_quant_staged.cuh",
                 "nvfp4_quant_gb300/csrc/rq_norm_quant_launch.cuh",
                 "nvfp4_quant_gb300/csrc/rq_norm_quant_bf16.cu"]
-_QK_SOURCES = ["include/rq.h", "nvfp4_quant_gb300/csrc/rq_api.cu", "nvfp4_quant_gb300/csrc/rq_launch.h",
+_QK_SOURCES = ["include/rq.h", "nvfp4_quant_gb300/csrc/rq_launch.h",
                "nvfp4_quant_gb300/csrc/rq_device.cuh", "nvfp4_quant_gb300/csrc/rq_qk.cu"]
 KERNEL_SOURCES = {"add_rmsnorm_nvfp4": _ROW_SOURCES, "add_rmsnorm_fp8": _ROW_SOURCES,
                   "add_rmsnorm_nvfp4_swizzled": _ROW_SOURCES, "qk_rmsnorm_rope_fp8": _QK_SOURCES}

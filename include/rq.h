@@ -65,6 +65,7 @@ typedef enum { RQ_BF16 = 0, RQ_FP16 = 1 } rq_dtype;
 
 #define RQ_MAX_HIDDEN 32768
 #define RQ_QK_HEAD_DIM 128
+#define RQ_QK_MAX_HEADS 65536
 
 /*
  * Residual add + RMSNorm + per-tensor FP8 E4M3.
@@ -130,6 +131,8 @@ rq_status rq_add_rmsnorm_nvfp4(const void *x, const void *residual_in,
  *   head_dim            must be RQ_QK_HEAD_DIM (128)
  *   n_q_heads or n_k_heads may be 0, in which case that side's pointers may
  *   be NULL.
+ * Limits (RQ_ERR_SHAPE beyond them): n_tokens <= 2^36, heads per side <=
+ * RQ_QK_MAX_HEADS, max_pos, token strides and num_slots <= 2^40.
  * Per head: n = dt(RMSNorm(x) * w); o_i = dt(n_i c_i - n_{i+64} s_i),
  * o_{i+64} = dt(n_{i+64} c_i + n_i s_i); out = E4M3(o / scale).
  */

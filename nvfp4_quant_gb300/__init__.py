@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(HERE, "lib", "librq.so")
 RQ_BF16, RQ_FP16 = 0, 1
 RQ_MAX_HIDDEN = 32768
 RQ_QK_HEAD_DIM = 128
+RQ_QK_MAX_HEADS = 65536
 STATUS = {0: "RQ_OK", 1: "RQ_ERR_NULL", 2: "RQ_ERR_SHAPE", 3: "RQ_ERR_DTYPE",
           4: "RQ_ERR_MISALIGNED", 5: "RQ_ERR_ALIAS", 6: "RQ_ERR_UNSUPPORTED", 7: "RQ_ERR_CUDA"}
 

@@ -339,7 +339,11 @@ static rq_status qk_call(const void *q, const void *k, int64_t q_token_stride,
                          rq_stream_t stream)
 {
     if (dt != RQ_BF16 && dt != RQ_FP16) return RQ_ERR_DTYPE;
-    if (n_tokens < 0 || n_q_heads < 0 || n_k_heads < 0 || max_pos < 1 || n_tokens > (int64_t)1 << 36)
+    // limits that keep every byte extent below 2^63 and the head count in an int
+    if (n_tokens < 0 || n_q_heads < 0 || n_k_heads < 0 || max_pos < 1 || n_tokens > (int64_t)1 << 36 ||
+        n_q_heads > RQ_QK_MAX_HEADS || n_k_heads > RQ_QK_MAX_HEADS || max_pos > (int64_t)1 << 40 ||
+        q_token_stride > (int64_t)1 << 40 || k_token_stride > (int64_t)1 << 40 ||
+        (k_slots && num_slots > (int64_t)1 << 40))
         return RQ_ERR_SHAPE;
     if (head_dim != RQ_QK_HEAD_DIM) return RQ_ERR_UNSUPPORTED;
     if (n_tokens == 0 || (n_q_heads == 0 && n_k_heads == 0)) return RQ_OK;

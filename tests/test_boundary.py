@@ -162,6 +162,10 @@ def test_qk_rejections(L):
     assert qk(L, qo=A["qo"] + 8) == MISAL
     assert qk(L, ko=A["qo"] + 32 * 16 * 128 - 16) == ALIAS
     assert qk(L, qo=A["cs"]) == ALIAS
+    # limits that keep byte extents in range
+    assert qk(L, maxp=(1 << 40) + 1) == SHAPE
+    assert qk(L, qst=(1 << 40) + 8) == SHAPE
+    assert qk(L, hq=65537, qst=65537 * 128) == SHAPE
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
