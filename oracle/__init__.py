@@ -51,6 +51,10 @@ def lib():
                                                 u16p, u16p, u8p, u8p]),
             "oracle_amax": (ctypes.c_float, [i32, u16p, i64]),
             "oracle_nvfp4_swizzled_scale_bytes": (i64, [i64, i64]),
+            "oracle_silu_dt": (ctypes.c_uint16, [i32, ctypes.c_uint16]),
+            "oracle_gated_rmsnorm": (None, [i32, u16p, u16p, u16p, f32, i64, i64, u16p, u16p]),
+            "oracle_gated_rmsnorm_nvfp4": (None, [i32, u16p, u16p, u16p, f32, f32, i64, i64,
+                                                  u16p, u16p, u8p, u8p]),
             "oracle_nvfp4_swizzle_scales": (None, [u8p, i64, i64, u8p]),
             "oracle_fp8_scale_from_amax": (ctypes.c_float, [f32]),
             "oracle_fp8_dynamic_scale": (ctypes.c_float, [f32]),
@@ -177,6 +181,39 @@ def add_rmsnorm_nvfp4(dt, x, r, w, eps, gs):
                                    _p(s, ctypes.c_uint16), _p(y, ctypes.c_uint16),
                                    _p(packed, ctypes.c_uint8), _p(sf, ctypes.c_uint8))
     return s, y, packed, sf
+
+
+def silu_dt(dt, z):
+    """dt(silu(z)) for every element of a uint16 array of dtype bits."""
+    z = np.asarray(z, np.uint16)
+    L = lib()
+    return np.fromiter((L.oracle_silu_dt(_DT[dt], int(b)) for b in z.ravel()), np.uint16,
+                       count=z.size).reshape(z.shape)
+
+
+def gated_rmsnorm(dt, x, z, w, eps):
+    """(g, y) of the gated RMSNorm: g = dt(x * silu(z)), y = RMSNorm(g) * w."""
+    x, z, w = _u16(x), _u16(z), _u16(w)
+    rows, hidden = x.shape
+    g, y = np.empty_like(x), np.empty_like(x)
+    lib().oracle_gated_rmsnorm(_DT[dt], _p(x, ctypes.c_uint16), _p(z, ctypes.c_uint16),
+                               _p(w, ctypes.c_uint16), eps, rows, hidden, _p(g, ctypes.c_uint16),
+                               _p(y, ctypes.c_uint16))
+    return g, y
+
+
+def gated_rmsnorm_nvfp4(dt, x, z, w, eps, gs):
+    """(g, y, packed codes, block scales) of the gated RMSNorm + NVFP4 call."""
+    x, z, w = _u16(x), _u16(z), _u16(w)
+    rows, hidden = x.shape
+    g, y = np.empty_like(x), np.empty_like(x)
+    packed = np.empty((rows, hidden // 2), np.uint8)
+    sf = np.empty((rows, hidden // 16), np.uint8)
+    lib().oracle_gated_rmsnorm_nvfp4(_DT[dt], _p(x, ctypes.c_uint16), _p(z, ctypes.c_uint16),
+                                     _p(w, ctypes.c_uint16), eps, gs, rows, hidden,
+                                     _p(g, ctypes.c_uint16), _p(y, ctypes.c_uint16),
+                                     _p(packed, ctypes.c_uint8), _p(sf, ctypes.c_uint8))
+    return g, y, packed, sf
 
 
 def amax(dt, v):

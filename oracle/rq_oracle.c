@@ -170,6 +170,26 @@ static float rms_rstd(double sum_sq, int64_t n, float eps)
     return rstd;
 }
 
+/* RMSNorm of one stored row s (steps 2 and 3 below): the sum of squares of
+ * s, rstd, then y = (s * rstd) * weight stored in dtype (if y is given). */
+static void rmsnorm_row(int dt, const uint16_t *sr, const uint16_t *w, float eps,
+                        int64_t hidden, uint16_t *yr)
+{
+    double sum_sq = 0.0;
+    for (int64_t i = 0; i < hidden; ++i) {
+        double v = (double)ld_dt(dt, sr[i]);
+        sum_sq += v * v;
+    }
+    float rstd = rms_rstd(sum_sq, hidden, eps);
+    if (yr) {
+        for (int64_t i = 0; i < hidden; ++i) {
+            float t = ld_dt(dt, sr[i]) * rstd;
+            float u = t * ld_dt(dt, w[i]);
+            yr[i] = st_dt(dt, u);
+        }
+    }
+}
+
 /* ---- residual add + RMSNorm ([P2] fused add + RMSNorm, [P4] local tail) ---- */
 void oracle_add_rmsnorm(int dt, const uint16_t *x, const uint16_t *r,
                         const uint16_t *w, float eps, int64_t rows,
@@ -189,24 +209,48 @@ void oracle_add_rmsnorm(int dt, const uint16_t *x, const uint16_t *r,
             sr[i] = st_dt(dt, sum);
         }
 
-        /* step 2: sum of squares of the stored residual', then rstd */
-        double sum_sq = 0.0;
-        for (int64_t i = 0; i < hidden; ++i) {
-            double v = (double)ld_dt(dt, sr[i]);
-            sum_sq += v * v;
-        }
-        float rstd = rms_rstd(sum_sq, hidden, eps);
-
-        /* step 3: y = (residual' * rstd) * weight, stored in dtype */
-        if (y_out) {
-            uint16_t *yr = y_out + row * hidden;
-            for (int64_t i = 0; i < hidden; ++i) {
-                float t = ld_dt(dt, sr[i]) * rstd;
-                float u = t * ld_dt(dt, w[i]);
-                yr[i] = st_dt(dt, u);
-            }
-        }
+        /* steps 2 and 3: rstd from the stored residual', then y */
+        rmsnorm_row(dt, sr, w, eps, hidden, y_out ? y_out + row * hidden : 0);
     }
+}
+
+/* ---- gated RMSNorm ([P2] the fused gated RMSNorm + NVFP4 op) ---- */
+uint16_t oracle_silu_dt(int dt, uint16_t z)
+{
+    double zz = dt == RQO_BF16 ? oracle_bf16_to_double(z) : oracle_fp16_to_double(z);
+    double v = zz / (1.0 + exp(-zz));  /* z * sigmoid(z); -0 when e^-z overflows */
+    return st_dt(dt, (float)v);        /* fp32, then the storage dtype */
+}
+
+void oracle_gated_rmsnorm(int dt, const uint16_t *x, const uint16_t *z,
+                          const uint16_t *w, float eps, int64_t rows,
+                          int64_t hidden, uint16_t *g_out, uint16_t *y_out)
+{
+    for (int64_t row = 0; row < rows; ++row) {
+        const uint16_t *xr = x + row * hidden;
+        const uint16_t *zr = z + row * hidden;
+        uint16_t *gr = g_out + row * hidden;
+
+        /* step 1: g = x * silu(z), one fp32 multiply, stored in dtype */
+        for (int64_t i = 0; i < hidden; ++i) {
+            float a = ld_dt(dt, xr[i]);
+            float b = ld_dt(dt, oracle_silu_dt(dt, zr[i]));
+            float prod = a * b;
+            gr[i] = st_dt(dt, prod);
+        }
+
+        /* steps 2 and 3 on g */
+        rmsnorm_row(dt, gr, w, eps, hidden, y_out ? y_out + row * hidden : 0);
+    }
+}
+
+void oracle_gated_rmsnorm_nvfp4(int dt, const uint16_t *x, const uint16_t *z,
+                                const uint16_t *w, float eps, float gs,
+                                int64_t rows, int64_t hidden, uint16_t *g_out,
+                                uint16_t *y_out, uint8_t *packed, uint8_t *sf)
+{
+    oracle_gated_rmsnorm(dt, x, z, w, eps, rows, hidden, g_out, y_out);
+    oracle_quant_nvfp4(dt, y_out, rows, hidden, gs, packed, sf);
 }
 
 /* ---- per-tensor FP8 E4M3 ([P1] RMSNorm with FP8 quantisation) ---- */

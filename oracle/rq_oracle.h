@@ -97,6 +97,23 @@ void oracle_add_rmsnorm_nvfp4(int dt, const uint16_t *x, const uint16_t *r,
                               int64_t rows, int64_t hidden, uint16_t *s_out,
                               uint16_t *y_out, uint8_t *packed, uint8_t *sf);
 
+/* Gated RMSNorm + NVFP4 ([P2] Changes: the fused gated RMSNorm + NVFP4 op;
+ * its formula is not on the page).  Reading: the separated sequence the
+ * fused op replaces, gate applied before the norm, one norm group per row,
+ * no residual:
+ *   silu(z) = z / (1 + e^-z), rounded to fp32 and then to the dtype
+ *   g_i     = dt(f32(x_i * silu(z_i)))                  -> g_out
+ *   then the RMSNorm steps above with residual' := g    -> y_out
+ *   and oracle_quant_nvfp4 on y (the _nvfp4 variant). */
+uint16_t oracle_silu_dt(int dt, uint16_t z);
+void oracle_gated_rmsnorm(int dt, const uint16_t *x, const uint16_t *z,
+                          const uint16_t *w, float eps, int64_t rows,
+                          int64_t hidden, uint16_t *g_out, uint16_t *y_out);
+void oracle_gated_rmsnorm_nvfp4(int dt, const uint16_t *x, const uint16_t *z,
+                                const uint16_t *w, float eps, float gs,
+                                int64_t rows, int64_t hidden, uint16_t *g_out,
+                                uint16_t *y_out, uint8_t *packed, uint8_t *sf);
+
 /* GEMM-facing block-scale layout.  The pages size the block-scale tensor for
  * the GEMM that consumes it ("Add AutoDeploy NVFP4 RMSNorm quant fusion",
  * review: the sf_size math of the shape-only ops; "[Performance]: Fuse local
