@@ -349,8 +349,9 @@ def measure_next_rows(wl, peak_kind_gbs, iters=50):
     workload, per-tensor dynamic FP8 / NVFP4 (amax pass + fused pass) on the
     prefill / large NVFP4 workloads, the large NVFP4 call with its block
     scales in the swizzled GEMM layout (same bytes: 16,384 rows and 7168
-    columns need no padding), and the Q/K call storing K into a KV pool of
-    8192 slots at shuffled slot indices."""
+    columns need no padding), the gated RMSNorm + NVFP4 call on the same
+    rows (the residual as the gate), and the Q/K call storing K into a KV
+    pool of 8192 slots at shuffled slot indices."""
     rq, d = wl.rq, wl.d
     f = lambda: torch.zeros(1, dtype=torch.float32, device="cuda")
     row_scales = torch.empty(FP8_ROWS, dtype=torch.float32, device="cuda")
@@ -372,6 +373,9 @@ def measure_next_rows(wl, peak_kind_gbs, iters=50):
         ("add_rmsnorm_nvfp4_swizzled", NV_ROWS, alg_bytes_nvfp4(NV_ROWS, NV_H),
          lambda: rq.rq_add_rmsnorm_nvfp4_swizzled(d["x5"], d["r5"], wl.ro5, wl.w5, EPS, wl.gs5,
                                                   wl.p5, sf_swz, wl.y5)),
+        # gated: read x and the gate z, write codes and scales (no residual, no norm out)
+        ("gated_rmsnorm_nvfp4", NV_ROWS, NV_ROWS * NV_H * (4 + 0.5 + 1 / 16) + NV_H * 2 + 4,
+         lambda: rq.rq_gated_rmsnorm_nvfp4(d["x5"], d["r5"], wl.w5, EPS, wl.gs5, wl.p5, wl.sf5)),
     ]
     n_slots = 2 * QK_T
     pool = torch.empty((n_slots, QK_HK, QK_D), dtype=torch.uint8, device="cuda")

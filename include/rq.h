@@ -169,6 +169,32 @@ rq_status rq_qk_rmsnorm_rope_fp8_kv_store(
     rq_stream_t stream);
 
 /*
+ * Gated RMSNorm + NVFP4: the NVFP4 call with the residual add replaced by a
+ * SiLU gate applied before the norm, and nothing written back:
+ *   g_i = dt(x_i * dt(silu(z_i))),  silu(z) = z / (1 + e^-z)
+ *   y_i = dt((g_i * rstd) * w_i),   rstd = 1 / sqrt(sum_i g_i^2 / hidden + eps)
+ * then the NVFP4 steps of rq_add_rmsnorm_nvfp4 on y (linear block scales).
+ * Source: "Add AutoDeploy NVFP4 RMSNorm quant fusion", Changes: the fused
+ * gated RMSNorm + NVFP4 op.  The page does not give the gating formula; the
+ * one above is the separated sequence such an op replaces (gate, then the
+ * norm over the whole row).  The kernel's fp32 SiLU is within 5 ulp of the
+ * correctly rounded value (measured over every fp32 input), so where that
+ * value lies next to a dtype rounding boundary, dt(silu(z)) can be one dtype
+ * step from the correctly rounded one (1 of the 65,536 bf16 values, 1 of the
+ * fp16 values).
+ *   x, z          [rows, hidden] dt, read
+ *   norm_out      [rows, hidden] dt, written with y; may be NULL
+ *   other arguments as in rq_add_rmsnorm_nvfp4; no output may overlap an
+ *   input.
+ */
+rq_status rq_gated_rmsnorm_nvfp4(const void *x, const void *z,
+                                 const void *weight, float eps,
+                                 const float *d_global_scale,
+                                 uint8_t *q_packed, uint8_t *block_scales,
+                                 void *norm_out, int64_t rows, int64_t hidden,
+                                 rq_dtype dt, rq_stream_t stream);
+
+/*
  * Calibration: d_amax = max over the tensor of |y| (the norm output the
  * fused calls would produce), written to one device fp32.  Nothing else is
  * written.  The call clears d_amax on `stream` first (so an empty tensor

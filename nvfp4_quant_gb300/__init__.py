@@ -50,6 +50,8 @@ SIGNATURES = {
     "rq_add_rmsnorm_nvfp4_dynamic_swizzled": (_int, [_vp, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _vp,
                                                      _i64, _i64, _int, _vp]),
     "rq_nvfp4_swizzled_scale_bytes": (ctypes.c_size_t, [_i64, _i64]),
+    "rq_gated_rmsnorm_nvfp4": (_int, [_vp, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _i64, _i64, _int,
+                                      _vp]),
     "rq_status_string": (ctypes.c_char_p, [_int]),
     "rq_last_error": (ctypes.c_char_p, []),
     "rq_version": (_int, []),
@@ -149,6 +151,20 @@ def rq_add_rmsnorm_nvfp4(x, residual_in, residual_out, weight, eps, global_scale
                                       _ptr(weight), float(eps), _ptr(global_scale),
                                       _ptr(q_packed), _ptr(block_scales), _ptr(norm_out),
                                       rows, hidden, _dt(x), _stream(stream)))
+
+
+def rq_gated_rmsnorm_nvfp4(x, z, weight, eps, global_scale, q_packed, block_scales,
+                           norm_out=None, stream=None):
+    """Gated RMSNorm + NVFP4 (include/rq.h): g = dt(x * dt(silu(z))), RMSNorm,
+    NVFP4.  q_packed: uint8 [rows, hidden/2]; block_scales: uint8 [rows, hidden/16]."""
+    rows, hidden = _rows(x, z, norm_out)
+    if weight.dtype != x.dtype:
+        raise ValueError("weight dtype must match x")
+    _out(q_packed, rows * hidden // 2, "q_packed")
+    _out(block_scales, rows * (hidden // 16), "block_scales")
+    _check(lib().rq_gated_rmsnorm_nvfp4(_ptr(x), _ptr(z), _ptr(weight), float(eps),
+                                        _ptr(global_scale), _ptr(q_packed), _ptr(block_scales),
+                                        _ptr(norm_out), rows, hidden, _dt(x), _stream(stream)))
 
 
 def rq_add_rmsnorm_amax(x, residual_in, weight, eps, amax_out, stream=None):

@@ -233,6 +233,27 @@ rq_status rq_add_rmsnorm_nvfp4_swizzled(const void *x, const void *residual_in, 
                       block_scales, norm_out, rows, hidden, dt, stream, 1);
 }
 
+rq_status rq_gated_rmsnorm_nvfp4(const void *x, const void *z, const void *weight, float eps,
+                                 const float *d_global_scale, uint8_t *q_packed,
+                                 uint8_t *block_scales, void *norm_out, int64_t rows,
+                                 int64_t hidden, rq_dtype dt, rq_stream_t stream)
+{
+    rq_status st = check_rows(rows, hidden, dt);
+    if (st != RQ_OK || rows == 0) return st;
+    if (!x || !z || !weight || !d_global_scale || !q_packed || !block_scales) return RQ_ERR_NULL;
+    if (!aligned16(x) || !aligned16(z) || !aligned16(weight) || !aligned16(q_packed) ||
+        !aligned16(block_scales) || (norm_out && !aligned16(norm_out)) || !aligned4(d_global_scale))
+        return RQ_ERR_MISALIGNED;
+    const int64_t tb = rows * hidden * 2;
+    const Span ins[] = {span(x, tb), span(z, tb), span(weight, hidden * 2), span(d_global_scale, 4)};
+    const Span outs[] = {span(norm_out, tb), span(q_packed, rows * hidden / 2),
+                         span(block_scales, sf_bytes(rows, hidden, 0))};
+    if (bad_alias(outs, 3, ins, 4)) return RQ_ERR_ALIAS;
+    auto p = make_params(x, z, nullptr, weight, eps, d_global_scale, q_packed, block_scales,
+                         norm_out, nullptr, rows, hidden);
+    return launch_rows<rq::MODE_GATED_NVFP4>(p, dt, stream);
+}
+
 rq_status rq_add_rmsnorm_amax(const void *x, const void *residual_in, const void *weight, float eps,
                               float *d_amax, int64_t rows, int64_t hidden, rq_dtype dt,
                               rq_stream_t stream)

@@ -52,10 +52,23 @@ struct QKParams {
 
 // MODE_NVFP4 writes the block scales row-major [rows, H/16]; MODE_NVFP4_SWZ
 // writes them in the 128 x 4-tile layout of block-scaled GEMMs (sf_offset).
-enum QuantMode { MODE_FP8 = 0, MODE_NVFP4 = 1, MODE_AMAX = 2, MODE_FP8_ROW = 3, MODE_NVFP4_SWZ = 4 };
+// MODE_GATED_NVFP4 replaces the residual add by the gate
+// g = dt(x * dt(silu(z))) (z in res_in; nothing written back) and quantises
+// like MODE_NVFP4.
+enum QuantMode {
+    MODE_FP8 = 0,
+    MODE_NVFP4 = 1,
+    MODE_AMAX = 2,
+    MODE_FP8_ROW = 3,
+    MODE_NVFP4_SWZ = 4,
+    MODE_GATED_NVFP4 = 5
+};
 
 template <int MODE>
-__host__ __device__ constexpr bool is_nvfp4() { return MODE == MODE_NVFP4 || MODE == MODE_NVFP4_SWZ; }
+__host__ __device__ constexpr bool is_nvfp4()
+{
+    return MODE == MODE_NVFP4 || MODE == MODE_NVFP4_SWZ || MODE == MODE_GATED_NVFP4;
+}
 
 // SM count of device `dev` (cached).
 int device_sms(int dev);

@@ -153,21 +153,30 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
             }
         }
 
-        // ---- residual' = dt(x + r), stored; sum of squares of the rounded values
+        // ---- residual' = dt(x + r), stored (gated: g = dt(x * dt(silu(z))),
+        // not stored); sum of squares of the rounded values
         float ss = 0.0f;
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
             float a[8], b[8];
             unpack8<DT>(xv[j], a);
             unpack8<DT>(sv[j], b);
+            if (MODE == MODE_GATED_NVFP4) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) a[e] = __fadd_rn(a[e], b[e]);
+                for (int e = 0; e < 8; ++e) b[e] = silu_f32(b[e]);
+                unpack8<DT>(pack8<DT>(b), b);  // the gate rounded to the dtype
+#pragma unroll
+                for (int e = 0; e < 8; ++e) a[e] = __fmul_rn(a[e], b[e]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) a[e] = __fadd_rn(a[e], b[e]);
+            }
             sv[j] = pack8<DT>(a);
             unpack8<DT>(sv[j], a);
 #pragma unroll
             for (int e = 0; e < 8; ++e) ss = __fmaf_rn(a[e], a[e], ss);  // squares are exact
             const int k = j * G + t;
-            if (MODE != MODE_AMAX && row_ok && k < nvec)
+            if (MODE != MODE_AMAX && MODE != MODE_GATED_NVFP4 && row_ok && k < nvec)
                 st16(static_cast<uint8_t *>(p.res_out) + (row * H + (int64_t)k * 8) * 2, sv[j]);
         }
 

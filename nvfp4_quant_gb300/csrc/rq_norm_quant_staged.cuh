@@ -9,7 +9,9 @@
 // residual' = dt(x + r), stores it, writes it back over the residual slot and
 // sums its squares; after the row reduction pass 2 normalises from shared
 // memory and quantises exactly as the register-resident kernel does (same
-// pairing of NVFP4 block halves in neighbouring lanes, same stores).
+// pairing of NVFP4 block halves in neighbouring lanes, same stores).  In the
+// gated mode the residual slot holds the gate z and pass 1 forms
+// g = dt(x * dt(silu(z))) there instead, without writing it back.
 // Registers stay low, so shared memory (4 * hidden bytes per row) sets the
 // number of rows in flight per SM: three at hidden 16384.
 #pragma once
@@ -68,10 +70,18 @@ __device__ __forceinline__ void staged_body(const NormQuantParams &p, uint4 *buf
                 float a[8], b[8];
                 unpack8<DT>(lds16(xs + k), a);
                 unpack8<DT>(lds16(rs + k), b);
+                if (MODE == MODE_GATED_NVFP4) {  // g = dt(x * dt(silu(z)))
 #pragma unroll
-                for (int e = 0; e < 8; ++e) a[e] = __fadd_rn(a[e], b[e]);
+                    for (int e = 0; e < 8; ++e) b[e] = silu_f32(b[e]);
+                    unpack8<DT>(pack8<DT>(b), b);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) a[e] = __fmul_rn(a[e], b[e]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) a[e] = __fadd_rn(a[e], b[e]);
+                }
                 const uint4 sv = pack8<DT>(a);
-                if (MODE != MODE_AMAX)
+                if (MODE != MODE_AMAX && MODE != MODE_GATED_NVFP4)
                     st16(static_cast<uint8_t *>(p.res_out) + (row * H + (int64_t)k * 8) * 2, sv);
                 sts16(rs + k, sv);
                 unpack8<DT>(sv, a);

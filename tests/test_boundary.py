@@ -133,6 +133,21 @@ def test_swizzled_scale_size_and_rejections(L):
     assert nvfp4_swz(L, y=None, rows=0) == OK
 
 
+def test_gated_rejections(L):
+    g = lambda **kw: L.rq_gated_rmsnorm_nvfp4(
+        kw.get("x", A["x"]), kw.get("z", A["r"]), kw.get("w", A["w"]), 1e-6, kw.get("s", A["s"]),
+        kw.get("q", A["q"]), kw.get("sf", A["sf"]), kw.get("y", A["y"]), kw.get("rows", 16),
+        kw.get("hidden", 128), kw.get("dt", 0), None)
+    assert g(rows=0, x=None, z=None) == OK
+    assert g(z=None) == NULL
+    assert g(sf=None) == NULL
+    assert g(z=A["r"] + 8) == MISAL
+    assert g(hidden=40) == SHAPE
+    assert g(dt=3) == DTYPE
+    assert g(y=A["r"]) == ALIAS  # nothing may be written over the gate
+    assert g(q=A["x"] + 16) == ALIAS
+
+
 def test_amax_rejections(L):
     f = lambda **kw: L.rq_add_rmsnorm_amax(kw.get("x", A["x"]), kw.get("r", A["r"]), kw.get("w", A["w"]),
                                            1e-6, kw.get("amax", A["amax"]), kw.get("rows", 4),

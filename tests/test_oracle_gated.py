@@ -9,8 +9,9 @@ then the RMSNorm and NVFP4 steps of the plain path on g.
   ulp, silu(z) = -0 where e^-z overflows;
 - the gate reduces to the plain path: with z = 32 (silu(32) rounds to 32)
   and eps = 0, g = 32 x exactly and the norm output equals the plain
-  residual-add path's on x (zero residual), bit for bit, because every step
-  commutes with a power-of-two scaling;
+  residual-add path's on x with a residual of -0 (x + (-0) = x, signed zeros
+  included), bit for bit, because every step commutes with a power-of-two
+  scaling;
 - an all-zero gate gives zero rows: signed zero codes and zero block scales.
 """
 import numpy as np
@@ -64,7 +65,8 @@ def test_gate_of_32_reduces_to_the_plain_path(dt):
     rows, hidden = 24, 1040
     x, _, w = synth.rows_input(3, rows, hidden, dt)
     z = np.full((rows, hidden), synth.to_bits(np.array([32.0]), dt)[0], np.uint16)
-    zeros = np.zeros_like(x)
+    zeros = np.full_like(x, 0x8000)  # -0: x + (-0) = x, signed zeros included
+    x[0, :8] = [0x0000, 0x8000] * 4  # signed zeros in x keep their sign on both paths
     g, y = O.gated_rmsnorm(dt, x, z, w, 0.0)
     s_ref, y_ref = O.add_rmsnorm(dt, x, zeros, w, 0.0)
     assert np.array_equal(pins.bits_to_f64(g, dt), 32.0 * pins.bits_to_f64(x, dt))
