@@ -110,3 +110,56 @@ def test_concurrent_calls_from_two_threads():
         x, r, w = inputs[i]
         _, _, q_ref = O.add_rmsnorm_fp8("fp16", x, r, w, 1e-6, 0.03)
         assert_codes(results[i], q_ref, 0x80, "FP8 codes from thread %d" % i)
+
+
+def test_every_call_captures_into_one_graph():
+    """Every entry point (static, dynamic, per-token, swizzled, gated, Q/K,
+    KV pool) captured in one CUDA graph; a replay reproduces the eager
+    outputs bit for bit (the kernels are deterministic)."""
+    rows, H = 300, 2048
+    x, r, w = synth.rows_input(50, rows, H, "bf16")
+    xd, rd, wd = dev16(x, "bf16"), dev16(r, "bf16"), dev16(w, "bf16")
+    T, Hq, Hk, D = 64, 4, 2, 128
+    q, k, qw, kw, pos, cs = synth.qk_input(51, T, Hq, Hk, D, "bf16")
+    qd, kd, qwd, kwd = dev16(q, "bf16"), dev16(k, "bf16"), dev16(qw, "bf16"), dev16(kw, "bf16")
+    posd, csd = torch.from_numpy(pos).cuda(), torch.from_numpy(cs).cuda()
+    u8 = lambda *s: torch.empty(s, dtype=torch.uint8, device="cuda")
+    f32 = lambda n: torch.empty(n, dtype=torch.float32, device="cuda")
+    out = {"ro": torch.empty_like(rd), "y": torch.empty_like(rd), "q8": u8(rows, H),
+           "p": u8(rows, H // 2), "sf": u8(rows, H // 16),
+           "sfz": u8(rq.rq_nvfp4_swizzled_scale_bytes(rows, H)), "rs": f32(rows), "s1": f32(1),
+           "s2": f32(1), "am": f32(1), "gp": u8(rows, H // 2), "gsf": u8(rows, H // 16),
+           "qo": u8(T, Hq, D), "pool": u8(2 * T, Hk, D)}
+    gs, sc = f32dev(300.0), f32dev(0.02)
+    slots = torch.randperm(2 * T, generator=torch.Generator().manual_seed(1))[:T].cuda()
+
+    def calls():
+        rq.rq_add_rmsnorm_fp8(xd, rd, out["ro"], wd, 1e-6, sc, out["q8"], out["y"])
+        rq.rq_add_rmsnorm_nvfp4(xd, rd, out["ro"], wd, 1e-6, gs, out["p"], out["sf"], out["y"])
+        rq.rq_add_rmsnorm_nvfp4_dynamic_swizzled(xd, rd, out["ro"], wd, 1e-6, out["s1"], out["p"],
+                                                 out["sfz"])
+        rq.rq_add_rmsnorm_fp8_per_token(xd, rd, out["ro"], wd, 1e-6, out["q8"], out["rs"])
+        rq.rq_add_rmsnorm_fp8_dynamic(xd, rd, out["ro"], wd, 1e-6, out["s2"], out["q8"])
+        rq.rq_add_rmsnorm_amax(xd, rd, wd, 1e-6, out["am"])
+        rq.rq_gated_rmsnorm_nvfp4(xd, rd, wd, 1e-6, gs, out["gp"], out["gsf"])
+        rq.rq_qk_rmsnorm_rope_fp8_kv_store(qd, kd, qwd, kwd, 1e-6, posd, csd, sc, sc, out["qo"],
+                                           out["pool"], slots)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for t in out.values():
+            t.zero_()
+        calls()  # eager, also the first-call set-up
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    eager = {k: v.clone() for k, v in out.items()}
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        calls()
+    for t in out.values():
+        t.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    for key in out:
+        assert torch.equal(out[key], eager[key]), key
