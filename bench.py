@@ -606,11 +606,15 @@ KERNEL_SOURCES = {"add_rmsnorm_nvfp4": _ROW_SOURCES, "add_rmsnorm_fp8": _ROW_SOU
 
 
 def source_hash(kernel):
+    """Hash of the code (comments and whitespace removed) of those files."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(rel.encode() + f.read())
+        with open(os.path.join(ROOT, rel)) as f:
+            code = re.sub(r"/\*.*?\*/", " ", f.read(), flags=re.S)
+        code = re.sub(r"//[^\n]*", " ", code)
+        h.update(rel.encode() + " ".join(code.split()).encode())
     return h.hexdigest()[:16]
 
 

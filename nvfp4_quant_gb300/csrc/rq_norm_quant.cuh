@@ -66,13 +66,6 @@ __device__ __forceinline__ void sf_zero_pad_rows(const NormQuantParams &p)
     }
 }
 
-// Stores the block scale sfc of block column c = k / 2 (k = this lane's
-// vector index; the lanes of vectors k and k + 1 hold the same scale).  With
-// whole groups of four columns (hidden % 64 == 0) the lane of k % 8 == 0
-// stores the four scales of its group as one word, gathered from the lanes
-// 2, 4 and 6 above it; otherwise each even-k lane stores its byte, and in the
-// swizzled layout the lane of the last column also zeroes the padding
-// columns after it.  Every lane of the warp must call this (shuffles).
 // Swizzled layout: where the row's bytes of its first tile start (the row's
 // part of sf_offset); block column c adds (c / 4) * 512 + c % 4.  (Computing
 // it once per row at the top of the row loop, instead of at each store, made
@@ -82,6 +75,13 @@ __device__ __forceinline__ uint8_t *sf_swizzled_row(const NormQuantParams &p, in
     return p.sf + (((row >> 7) * p.sf_col_tiles) << 9) + ((row & 31) << 4) + (((row >> 5) & 3) << 2);
 }
 
+// Stores the block scale sfc of block column c = k / 2 (k = this lane's
+// vector index; the lanes of vectors k and k + 1 hold the same scale).  With
+// whole groups of four columns (hidden % 64 == 0) the lane of k % 8 == 0
+// stores the four scales of its group as one word, gathered from the lanes
+// 2, 4 and 6 above it; otherwise each even-k lane stores its byte, and in the
+// swizzled layout the lane of the last column also zeroes the padding
+// columns after it.  Every lane of the warp must call this (shuffles).
 template <bool kSwz>
 __device__ __forceinline__ void store_block_scale(const NormQuantParams &p, int64_t row, int k,
                                                   bool ok, uint32_t sfc, bool sf_words)
