@@ -30,8 +30,24 @@ def _nvcc():
     return "nvcc"
 
 
+# The row-kernel translation units hold one instantiation per quantisation
+# mode (rq::QuantMode, 0 .. 5); each mode is compiled as its own object, in
+# parallel, with -DRQ_MODE=<mode>.
+ROW_MODES = range(6)
+
+
 def sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+
+
+def _jobs():
+    jobs = []
+    for src in sources():
+        if os.path.basename(src).startswith("rq_norm_quant_"):
+            jobs += [(src, ["-DRQ_MODE=%d" % m], ".m%d" % m) for m in ROW_MODES]
+        else:
+            jobs.append((src, [], ""))
+    return jobs
 
 
 def _deps():
@@ -55,9 +71,10 @@ def build(force=False, verbose=False, ptxas_info=False):
     nvcc = _nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
 
-    def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-        cmd = [nvcc, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
+    def compile_one(job):
+        src, defs, tag = job
+        obj = os.path.join(BUILD, os.path.basename(src) + tag + ".o")
+        cmd = [nvcc, *NVCC_FLAGS, *defs, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("nvcc failed on %s:\n%s%s" % (src, r.stdout, r.stderr))
@@ -65,11 +82,13 @@ def build(force=False, verbose=False, ptxas_info=False):
             sys.stderr.write(r.stdout + r.stderr)
         return obj
 
-    srcs = sources()
-    with ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
-        objs = list(ex.map(compile_one, srcs))
+    jobs = _jobs()
+    with ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 1))) as ex:
+        objs = list(ex.map(compile_one, jobs))
     tmp = LIB + ".tmp.%d" % os.getpid()
-    cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
+    # -z defs: a mode left out of the objects fails here, not at load time
+    cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-Xlinker", "-z", "-Xlinker", "defs", "-o",
+           tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s%s" % (r.stdout, r.stderr))

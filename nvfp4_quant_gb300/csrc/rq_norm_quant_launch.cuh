@@ -119,6 +119,11 @@ cudaError_t launch_add_rmsnorm(const NormQuantParams &p, cudaStream_t stream)
 
 }  // namespace rq
 
+// One mode of one dtype (the build compiles each mode in its own translation
+// unit, in parallel, with -DRQ_MODE=<mode>), or all of them.
+#define RQ_INSTANTIATE_MODE(DT, MODE)                                                          \
+    template cudaError_t rq::launch_add_rmsnorm<DT, MODE>(const rq::NormQuantParams &, cudaStream_t);
+
 #define RQ_INSTANTIATE_NORM_QUANT(DT)                                                          \
     template cudaError_t rq::launch_add_rmsnorm<DT, rq::MODE_FP8>(const rq::NormQuantParams &, \
                                                                   cudaStream_t);               \
