@@ -602,7 +602,8 @@ _ROW_SOURCES = ["include/rq.h", "nvfp4_quant_gb300/csrc/rq_launch.h",
 _QK_SOURCES = ["include/rq.h", "nvfp4_quant_gb300/csrc/rq_launch.h",
                "nvfp4_quant_gb300/csrc/rq_device.cuh", "nvfp4_quant_gb300/csrc/rq_qk.cu"]
 KERNEL_SOURCES = {"add_rmsnorm_nvfp4": _ROW_SOURCES, "add_rmsnorm_fp8": _ROW_SOURCES,
-                  "add_rmsnorm_nvfp4_swizzled": _ROW_SOURCES, "qk_rmsnorm_rope_fp8": _QK_SOURCES}
+                  "add_rmsnorm_nvfp4_swizzled": _ROW_SOURCES, "gated_rmsnorm_nvfp4": _ROW_SOURCES,
+                  "qk_rmsnorm_rope_fp8": _QK_SOURCES}
 
 
 def source_hash(kernel):
