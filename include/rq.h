@@ -193,6 +193,16 @@ rq_status rq_gated_rmsnorm_nvfp4(const void *x, const void *z,
                                  uint8_t *q_packed, uint8_t *block_scales,
                                  void *norm_out, int64_t rows, int64_t hidden,
                                  rq_dtype dt, rq_stream_t stream);
+/* The same with the block scales in the swizzled layout of
+ * rq_add_rmsnorm_nvfp4_swizzled (rq_nvfp4_swizzled_scale_bytes bytes, every
+ * byte written, padding 0). */
+rq_status rq_gated_rmsnorm_nvfp4_swizzled(const void *x, const void *z,
+                                          const void *weight, float eps,
+                                          const float *d_global_scale,
+                                          uint8_t *q_packed,
+                                          uint8_t *block_scales, void *norm_out,
+                                          int64_t rows, int64_t hidden,
+                                          rq_dtype dt, rq_stream_t stream);
 
 /*
  * Calibration: d_amax = max over the tensor of |y| (the norm output the

@@ -52,6 +52,8 @@ SIGNATURES = {
     "rq_nvfp4_swizzled_scale_bytes": (ctypes.c_size_t, [_i64, _i64]),
     "rq_gated_rmsnorm_nvfp4": (_int, [_vp, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _i64, _i64, _int,
                                       _vp]),
+    "rq_gated_rmsnorm_nvfp4_swizzled": (_int, [_vp, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _i64, _i64,
+                                               _int, _vp]),
     "rq_status_string": (ctypes.c_char_p, [_int]),
     "rq_last_error": (ctypes.c_char_p, []),
     "rq_version": (_int, []),
@@ -165,6 +167,20 @@ def rq_gated_rmsnorm_nvfp4(x, z, weight, eps, global_scale, q_packed, block_scal
     _check(lib().rq_gated_rmsnorm_nvfp4(_ptr(x), _ptr(z), _ptr(weight), float(eps),
                                         _ptr(global_scale), _ptr(q_packed), _ptr(block_scales),
                                         _ptr(norm_out), rows, hidden, _dt(x), _stream(stream)))
+
+
+def rq_gated_rmsnorm_nvfp4_swizzled(x, z, weight, eps, global_scale, q_packed, block_scales,
+                                    norm_out=None, stream=None):
+    """rq_gated_rmsnorm_nvfp4 with swizzled block scales (include/rq.h);
+    block_scales: uint8 of rq_nvfp4_swizzled_scale_bytes(rows, hidden) bytes."""
+    rows, hidden = _rows(x, z, norm_out)
+    if weight.dtype != x.dtype:
+        raise ValueError("weight dtype must match x")
+    _out(q_packed, rows * hidden // 2, "q_packed")
+    _out(block_scales, rq_nvfp4_swizzled_scale_bytes(rows, hidden), "block_scales")
+    _check(lib().rq_gated_rmsnorm_nvfp4_swizzled(
+        _ptr(x), _ptr(z), _ptr(weight), float(eps), _ptr(global_scale), _ptr(q_packed),
+        _ptr(block_scales), _ptr(norm_out), rows, hidden, _dt(x), _stream(stream)))
 
 
 def rq_add_rmsnorm_amax(x, residual_in, weight, eps, amax_out, stream=None):

@@ -31,9 +31,9 @@ def _nvcc():
 
 
 # The row-kernel translation units hold one instantiation per quantisation
-# mode (rq::QuantMode, 0 .. 5); each mode is compiled as its own object, in
+# mode (rq::QuantMode, 0 .. 6); each mode is compiled as its own object, in
 # parallel, with -DRQ_MODE=<mode>.
-ROW_MODES = range(6)
+ROW_MODES = range(7)
 
 
 def sources():

@@ -233,10 +233,10 @@ rq_status rq_add_rmsnorm_nvfp4_swizzled(const void *x, const void *residual_in, 
                       block_scales, norm_out, rows, hidden, dt, stream, 1);
 }
 
-rq_status rq_gated_rmsnorm_nvfp4(const void *x, const void *z, const void *weight, float eps,
-                                 const float *d_global_scale, uint8_t *q_packed,
-                                 uint8_t *block_scales, void *norm_out, int64_t rows,
-                                 int64_t hidden, rq_dtype dt, rq_stream_t stream)
+static rq_status gated_call(const void *x, const void *z, const void *weight, float eps,
+                            const float *d_global_scale, uint8_t *q_packed, uint8_t *block_scales,
+                            void *norm_out, int64_t rows, int64_t hidden, rq_dtype dt,
+                            rq_stream_t stream, int sf_swizzled)
 {
     rq_status st = check_rows(rows, hidden, dt);
     if (st != RQ_OK || rows == 0) return st;
@@ -247,11 +247,31 @@ rq_status rq_gated_rmsnorm_nvfp4(const void *x, const void *z, const void *weigh
     const int64_t tb = rows * hidden * 2;
     const Span ins[] = {span(x, tb), span(z, tb), span(weight, hidden * 2), span(d_global_scale, 4)};
     const Span outs[] = {span(norm_out, tb), span(q_packed, rows * hidden / 2),
-                         span(block_scales, sf_bytes(rows, hidden, 0))};
+                         span(block_scales, sf_bytes(rows, hidden, sf_swizzled))};
     if (bad_alias(outs, 3, ins, 4)) return RQ_ERR_ALIAS;
     auto p = make_params(x, z, nullptr, weight, eps, d_global_scale, q_packed, block_scales,
                          norm_out, nullptr, rows, hidden);
-    return launch_rows<rq::MODE_GATED_NVFP4>(p, dt, stream);
+    return sf_swizzled ? launch_rows<rq::MODE_GATED_NVFP4_SWZ>(p, dt, stream)
+                       : launch_rows<rq::MODE_GATED_NVFP4>(p, dt, stream);
+}
+
+rq_status rq_gated_rmsnorm_nvfp4(const void *x, const void *z, const void *weight, float eps,
+                                 const float *d_global_scale, uint8_t *q_packed,
+                                 uint8_t *block_scales, void *norm_out, int64_t rows,
+                                 int64_t hidden, rq_dtype dt, rq_stream_t stream)
+{
+    return gated_call(x, z, weight, eps, d_global_scale, q_packed, block_scales, norm_out, rows,
+                      hidden, dt, stream, 0);
+}
+
+rq_status rq_gated_rmsnorm_nvfp4_swizzled(const void *x, const void *z, const void *weight,
+                                          float eps, const float *d_global_scale,
+                                          uint8_t *q_packed, uint8_t *block_scales,
+                                          void *norm_out, int64_t rows, int64_t hidden,
+                                          rq_dtype dt, rq_stream_t stream)
+{
+    return gated_call(x, z, weight, eps, d_global_scale, q_packed, block_scales, norm_out, rows,
+                      hidden, dt, stream, 1);
 }
 
 rq_status rq_add_rmsnorm_amax(const void *x, const void *residual_in, const void *weight, float eps,

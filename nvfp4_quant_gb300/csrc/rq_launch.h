@@ -54,20 +54,34 @@ struct QKParams {
 // writes them in the 128 x 4-tile layout of block-scaled GEMMs (sf_offset).
 // MODE_GATED_NVFP4 replaces the residual add by the gate
 // g = dt(x * dt(silu(z))) (z in res_in; nothing written back) and quantises
-// like MODE_NVFP4.
+// like MODE_NVFP4; MODE_GATED_NVFP4_SWZ likewise, with swizzled scales.
 enum QuantMode {
     MODE_FP8 = 0,
     MODE_NVFP4 = 1,
     MODE_AMAX = 2,
     MODE_FP8_ROW = 3,
     MODE_NVFP4_SWZ = 4,
-    MODE_GATED_NVFP4 = 5
+    MODE_GATED_NVFP4 = 5,
+    MODE_GATED_NVFP4_SWZ = 6
 };
 
 template <int MODE>
 __host__ __device__ constexpr bool is_nvfp4()
 {
-    return MODE == MODE_NVFP4 || MODE == MODE_NVFP4_SWZ || MODE == MODE_GATED_NVFP4;
+    return MODE == MODE_NVFP4 || MODE == MODE_NVFP4_SWZ || MODE == MODE_GATED_NVFP4 ||
+           MODE == MODE_GATED_NVFP4_SWZ;
+}
+
+template <int MODE>
+__host__ __device__ constexpr bool is_gated()
+{
+    return MODE == MODE_GATED_NVFP4 || MODE == MODE_GATED_NVFP4_SWZ;
+}
+
+template <int MODE>
+__host__ __device__ constexpr bool is_swizzled()
+{
+    return MODE == MODE_NVFP4_SWZ || MODE == MODE_GATED_NVFP4_SWZ;
 }
 
 // SM count of device `dev` (cached).

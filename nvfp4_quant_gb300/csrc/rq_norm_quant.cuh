@@ -161,7 +161,7 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
             float a[8], b[8];
             unpack8<DT>(xv[j], a);
             unpack8<DT>(sv[j], b);
-            if (MODE == MODE_GATED_NVFP4) {
+            if (is_gated<MODE>()) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) b[e] = silu_f32(b[e]);
                 unpack8<DT>(pack8<DT>(b), b);  // the gate rounded to the dtype
@@ -176,7 +176,7 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
 #pragma unroll
             for (int e = 0; e < 8; ++e) ss = __fmaf_rn(a[e], a[e], ss);  // squares are exact
             const int k = j * G + t;
-            if (MODE != MODE_AMAX && MODE != MODE_GATED_NVFP4 && row_ok && k < nvec)
+            if (MODE != MODE_AMAX && !is_gated<MODE>() && row_ok && k < nvec)
                 st16(static_cast<uint8_t *>(p.res_out) + (row * H + (int64_t)k * 8) * 2, sv[j]);
         }
 
@@ -232,7 +232,7 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
                 for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(y[e], enc);
                 const uint32_t codes = e2m1x8(v);
                 if (ok) st4(p.q + row * (H / 2) + (int64_t)k * 4, codes);
-                store_block_scale<MODE == MODE_NVFP4_SWZ>(p, row, k, ok, sfc, sf_words);
+                store_block_scale<is_swizzled<MODE>()>(p, row, k, ok, sfc, sf_words);
             } else if (MODE == MODE_FP8_ROW) {
                 sv[j] = yv;  // residual' is stored; keep the rounded y for the second pass
                 if (ok) {
@@ -283,7 +283,7 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
         }
     }
 
-    if (MODE == MODE_NVFP4_SWZ) sf_zero_pad_rows(p);
+    if (is_swizzled<MODE>()) sf_zero_pad_rows(p);
 
     if (MODE == MODE_AMAX) {
         // block maximum, then one atomic per CTA on the float's bit pattern

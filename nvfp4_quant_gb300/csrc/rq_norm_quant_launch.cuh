@@ -136,4 +136,6 @@ cudaError_t launch_add_rmsnorm(const NormQuantParams &p, cudaStream_t stream)
     template cudaError_t rq::launch_add_rmsnorm<DT, rq::MODE_NVFP4_SWZ>(                       \
         const rq::NormQuantParams &, cudaStream_t);                                            \
     template cudaError_t rq::launch_add_rmsnorm<DT, rq::MODE_GATED_NVFP4>(                     \
+        const rq::NormQuantParams &, cudaStream_t);                                            \
+    template cudaError_t rq::launch_add_rmsnorm<DT, rq::MODE_GATED_NVFP4_SWZ>(                 \
         const rq::NormQuantParams &, cudaStream_t);

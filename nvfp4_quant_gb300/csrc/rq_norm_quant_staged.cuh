@@ -70,7 +70,7 @@ __device__ __forceinline__ void staged_body(const NormQuantParams &p, uint4 *buf
                 float a[8], b[8];
                 unpack8<DT>(lds16(xs + k), a);
                 unpack8<DT>(lds16(rs + k), b);
-                if (MODE == MODE_GATED_NVFP4) {  // g = dt(x * dt(silu(z)))
+                if (is_gated<MODE>()) {  // g = dt(x * dt(silu(z)))
 #pragma unroll
                     for (int e = 0; e < 8; ++e) b[e] = silu_f32(b[e]);
                     unpack8<DT>(pack8<DT>(b), b);
@@ -81,7 +81,7 @@ __device__ __forceinline__ void staged_body(const NormQuantParams &p, uint4 *buf
                     for (int e = 0; e < 8; ++e) a[e] = __fadd_rn(a[e], b[e]);
                 }
                 const uint4 sv = pack8<DT>(a);
-                if (MODE != MODE_AMAX && MODE != MODE_GATED_NVFP4)
+                if (MODE != MODE_AMAX && !is_gated<MODE>())
                     st16(static_cast<uint8_t *>(p.res_out) + (row * H + (int64_t)k * 8) * 2, sv);
                 sts16(rs + k, sv);
                 unpack8<DT>(sv, a);
@@ -134,7 +134,7 @@ __device__ __forceinline__ void staged_body(const NormQuantParams &p, uint4 *buf
                 for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(y[e], enc);
                 const uint32_t codes = e2m1x8(v);
                 if (ok) st4(p.q + row * (H / 2) + (int64_t)k * 4, codes);
-                store_block_scale<MODE == MODE_NVFP4_SWZ>(p, row, k, ok, sfc, sf_words);
+                store_block_scale<is_swizzled<MODE>()>(p, row, k, ok, sfc, sf_words);
             } else if (MODE == MODE_FP8_ROW) {
                 if (ok) {
                     sts16(xs + k, yv);  // the rounded y, for the pass after the row maximum
@@ -182,7 +182,7 @@ __device__ __forceinline__ void staged_body(const NormQuantParams &p, uint4 *buf
     cp_async_commit();
     cp_async_wait<0>();  // nothing may stay in flight at exit
 
-    if (MODE == MODE_NVFP4_SWZ) sf_zero_pad_rows(p);
+    if (is_swizzled<MODE>()) sf_zero_pad_rows(p);
 
     if (MODE == MODE_AMAX) {
         float m = group_max<32>(amax_acc);

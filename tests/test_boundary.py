@@ -146,6 +146,11 @@ def test_gated_rejections(L):
     assert g(dt=3) == DTYPE
     assert g(y=A["r"]) == ALIAS  # nothing may be written over the gate
     assert g(q=A["x"] + 16) == ALIAS
+    gz = lambda **kw: L.rq_gated_rmsnorm_nvfp4_swizzled(
+        A["x"], A["r"], A["w"], 1e-6, A["s"], A["q"], kw.get("sf", A["sf"]), None, 16, 128, 0, None)
+    assert gz(sf=None) == NULL
+    assert gz(sf=A["sf"] + 4) == MISAL
+    assert gz(sf=A["q"] - 512) == ALIAS  # the padded 1024-byte scale buffer reaches the codes
 
 
 def test_amax_rejections(L):

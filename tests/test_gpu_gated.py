@@ -163,3 +163,23 @@ def test_silu_error_over_every_fp32_input(tmp_path):
     assert v["max_ulp"] <= 5 and v["over4"] <= 1, out
     assert v["subnormal_max_ulp"] <= 2, out
     assert v["bf16_diff"] <= 2 and v["fp16_diff"] <= 2, out
+
+
+@pytest.mark.parametrize("rows,hidden,dt", [(130, 96, "bf16"), (300, 1056, "fp16"), (16384, 7168, "bf16"),
+                                            (-1, 16384, "bf16"), (5, 8208, "fp16")])
+def test_gated_swizzled_scales(rows, hidden, dt):
+    """The swizzled gated call: codes equal to the linear call's, scales byte
+    for byte the oracle's layout of the linear call's scales, padding zero
+    (the buffer is poisoned beforehand)."""
+    rows = 2 * SMS + 3 if rows == -1 else rows
+    x, z, w = synth.rows_input(rows + 3, rows, hidden, dt)
+    gs = gated_gs(dt, x, z, w, 1e-6)
+    _, p, sf = run_gated(dt, x, z, w, 1e-6, gs, norm_out=False)
+    xd, zd, wd = dev16(x, dt), dev16(z, dt), dev16(w, dt)
+    p2 = Guarded((rows, hidden // 2), torch.uint8)
+    sz = Guarded((rq.rq_nvfp4_swizzled_scale_bytes(rows, hidden),), torch.uint8)
+    rq.rq_gated_rmsnorm_nvfp4_swizzled(xd, zd, wd, 1e-6, f32dev(gs), p2.t, sz.t)
+    torch.cuda.synchronize()
+    assert p2.guards_intact() and sz.guards_intact(), "a kernel wrote outside its output"
+    assert np.array_equal(host8(p2.t), p)
+    assert np.array_equal(host8(sz.t), O.nvfp4_swizzle_scales(sf.reshape(rows, hidden // 16), hidden))
