@@ -129,7 +129,8 @@ def test_every_call_captures_into_one_graph():
            "p": u8(rows, H // 2), "sf": u8(rows, H // 16),
            "sfz": u8(rq.rq_nvfp4_swizzled_scale_bytes(rows, H)), "rs": f32(rows), "s1": f32(1),
            "s2": f32(1), "am": f32(1), "gp": u8(rows, H // 2), "gsf": u8(rows, H // 16),
-           "qo": u8(T, Hq, D), "pool": u8(2 * T, Hk, D)}
+           "qo": u8(T, Hq, D), "pool": u8(2 * T, Hk, D), "gzp": u8(rows, H // 2),
+           "gzs": u8(rq.rq_nvfp4_swizzled_scale_bytes(rows, H))}
     gs, sc = f32dev(300.0), f32dev(0.02)
     slots = torch.randperm(2 * T, generator=torch.Generator().manual_seed(1))[:T].cuda()
 
@@ -142,6 +143,7 @@ def test_every_call_captures_into_one_graph():
         rq.rq_add_rmsnorm_fp8_dynamic(xd, rd, out["ro"], wd, 1e-6, out["s2"], out["q8"])
         rq.rq_add_rmsnorm_amax(xd, rd, wd, 1e-6, out["am"])
         rq.rq_gated_rmsnorm_nvfp4(xd, rd, wd, 1e-6, gs, out["gp"], out["gsf"])
+        rq.rq_gated_rmsnorm_nvfp4_swizzled(xd, rd, wd, 1e-6, gs, out["gzp"], out["gzs"])
         rq.rq_qk_rmsnorm_rope_fp8_kv_store(qd, kd, qwd, kwd, 1e-6, posd, csd, sc, sc, out["qo"],
                                            out["pool"], slots)
 
