@@ -6,6 +6,9 @@ order that a block-scaled NVFP4 GEMM (cuBLASLt, 16-element blocks, E4M3
 scales) reads.  Its byte order is pinned on the GPU by feeding the oracle's
 output to that GEMM (tests/test_gpu_swizzle.py).  Here, without a GPU:
 
+- the byte of each scale agrees with offsets worked by hand from the
+  documented 128 x 4 block layout (tests/golden/nvfp4_swizzle_offsets.txt);
+
 - the padded size agrees with the shape rule torch applies before it calls
   that GEMM (its meta kernel, which runs on the CPU), and any other size is
   refused by it;
@@ -86,3 +89,46 @@ def test_values_survive_and_rows_of_tiles_are_contiguous():
     first = O.nvfp4_swizzle_scales(np.where(np.arange(rows)[:, None] < 128, sf, 0), hidden)
     assert np.array_equal(first[:per_tile_row], out[:per_tile_row])
     assert not first[per_tile_row:].any()
+
+
+def _golden_cases():
+    """Cases of tests/golden/nvfp4_swizzle_offsets.txt: (rows, hidden, size,
+    [(r, c, offset)], [padding offsets])."""
+    import os
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                        "nvfp4_swizzle_offsets.txt")
+    cases = []
+    with open(path) as f:
+        for line in f:
+            w = line.split()
+            if not w or w[0].startswith("#"):
+                continue
+            if w[0] == "case":
+                cases.append((int(w[1]), int(w[2]), int(w[3]), [], []))
+            elif w[0] == "at":
+                cases[-1][3].append((int(w[1]), int(w[2]), int(w[3])))
+            elif w[0] == "pad":
+                cases[-1][4].append(int(w[1]))
+    return cases
+
+
+@pytest.mark.parametrize("case", _golden_cases(), ids=lambda c: "%dx%d" % (c[0], c[1]))
+def test_byte_offsets_match_the_hand_worked_golden(case):
+    """Where each scale lands, against offsets worked by hand from the
+    documented 128 x 4 block layout (row of tiles outermost; inside a tile
+    (r, c) at 16 * (r mod 32) + 4 * (r div 32) + c)."""
+    rows, hidden, size, at, pad = case
+    nb = hidden // 16
+    assert O.nvfp4_swizzled_scale_bytes(rows, hidden) == size
+    # every scale a distinct nonzero byte, so a byte identifies its (r, c)
+    ids = (np.arange(rows * nb) % 251 + 1).astype(np.uint8).reshape(rows, nb)
+    out = O.nvfp4_swizzle_scales(ids, hidden)
+    assert out.size == size
+    for r, c, off in at:
+        assert out[off] == ids[r, c], "scale (%d, %d) is not at byte %d" % (r, c, off)
+        # and nowhere else among the bytes holding its id within its own tile
+        tile = off // 512
+        same = np.flatnonzero(out[tile * 512:(tile + 1) * 512] == ids[r, c]) + tile * 512
+        assert off in same
+    for off in pad:
+        assert out[off] == 0, "padding byte %d is not zero" % off
