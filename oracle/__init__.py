@@ -65,6 +65,8 @@ def lib():
                                               fp, i64, u16p]),
             "oracle_qk_rmsnorm_rope_fp8": (None, [i32, u16p, i64, i64, i32, i32, u16p, f32,
                                                   i32p, fp, i64, f32, u16p, u8p]),
+            "oracle_qk_rmsnorm_rope_partial": (None, [i32, u16p, i64, i64, i32, i32, i32, u16p,
+                                                      f32, i32p, fp, i64, u16p]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -279,6 +281,24 @@ def qk_rmsnorm_rope_fp8(dt, src, token_stride, n_tokens, n_heads, head_dim, w, e
                                      max_pos, scale, _p(o, ctypes.c_uint16),
                                      _p(q, ctypes.c_uint8))
     return o, q
+
+
+def qk_rmsnorm_rope_partial(dt, src, token_stride, n_tokens, n_heads, head_dim, rope_dim, w,
+                            eps, pos, cos_sin):
+    """Rounded values o [n_tokens, n_heads, head_dim] with the NeoX rotation on
+    the last rope_dim elements of each head only; cos_sin is [max_pos,
+    rope_dim]."""
+    src, w = _u16(src), _u16(w)
+    pos = np.ascontiguousarray(pos, dtype=np.int32)
+    cos_sin = np.ascontiguousarray(cos_sin, dtype=np.float32)
+    assert cos_sin.shape[1] == rope_dim
+    max_pos = cos_sin.shape[0]
+    o = np.empty((n_tokens, n_heads, head_dim), np.uint16)
+    lib().oracle_qk_rmsnorm_rope_partial(_DT[dt], _p(src, ctypes.c_uint16), token_stride, n_tokens,
+                                         n_heads, head_dim, rope_dim, _p(w, ctypes.c_uint16), eps,
+                                         _p(pos, ctypes.c_int32), _p(cos_sin, ctypes.c_float),
+                                         max_pos, _p(o, ctypes.c_uint16))
+    return o
 
 
 def nvfp4_swizzled_scale_bytes(rows, hidden):

@@ -429,3 +429,59 @@ void oracle_qk_rmsnorm_rope_fp8(int dt, const uint16_t *src,
                            w, eps, pos, cos_sin, max_pos, o);
     oracle_quant_fp8(dt, o, n_tokens * (int64_t)n_heads * head_dim, scale, q);
 }
+
+/* ---- Q/K RMSNorm + NeoX RoPE over the last rope_dim elements of each head
+ *      ([P3] review thread: the FlashMLA counterpart's fp8-nope + bf16-rope
+ *      KV pool; the split of the head is a reading) ---- */
+void oracle_qk_rmsnorm_rope_partial(int dt, const uint16_t *src,
+                                    int64_t token_stride, int64_t n_tokens,
+                                    int n_heads, int head_dim, int rope_dim,
+                                    const uint16_t *w, float eps,
+                                    const int32_t *pos, const float *cos_sin,
+                                    int64_t max_pos, uint16_t *o)
+{
+    const int nope = head_dim - rope_dim;
+    const int half = rope_dim / 2;
+    uint16_t n[1024];
+    if (head_dim <= 0 || head_dim > 1024 || rope_dim < 2 || rope_dim > head_dim ||
+        rope_dim % 2 != 0)
+        return;
+    for (int64_t t = 0; t < n_tokens; ++t) {
+        int64_t p = pos[t];
+        if (p < 0) p = 0;
+        if (p >= max_pos) p = max_pos - 1;
+        const float *cs = cos_sin + p * rope_dim;   /* rope_dim/2 cos, then sin */
+        for (int h = 0; h < n_heads; ++h) {
+            const uint16_t *xh = src + t * token_stride + (int64_t)h * head_dim;
+            uint16_t *oh = o + (t * n_heads + h) * (int64_t)head_dim;
+
+            /* RMSNorm over the whole head, rounded to dt */
+            double sum_sq = 0.0;
+            for (int i = 0; i < head_dim; ++i) {
+                double v = (double)ld_dt(dt, xh[i]);
+                sum_sq += v * v;
+            }
+            float rstd = rms_rstd(sum_sq, head_dim, eps);
+            for (int i = 0; i < head_dim; ++i) {
+                float a = ld_dt(dt, xh[i]) * rstd;
+                float b = a * ld_dt(dt, w[i]);
+                n[i] = st_dt(dt, b);
+            }
+
+            /* the first `nope` elements pass unrotated */
+            for (int i = 0; i < nope; ++i) oh[i] = n[i];
+
+            /* NeoX rotation of the pairs (nope + i, nope + half + i) */
+            for (int i = 0; i < half; ++i) {
+                float c = cs[i], s = cs[half + i];
+                float lo = ld_dt(dt, n[nope + i]), hi = ld_dt(dt, n[nope + half + i]);
+                float a1 = lo * c, a2 = hi * s;
+                float olo = a1 - a2;
+                float b1 = hi * c, b2 = lo * s;
+                float ohi = b1 + b2;
+                oh[nope + i] = st_dt(dt, olo);
+                oh[nope + half + i] = st_dt(dt, ohi);
+            }
+        }
+    }
+}

@@ -172,6 +172,28 @@ void oracle_qk_rmsnorm_rope_fp8(int dt, const uint16_t *src,
                                 const float *cos_sin, int64_t max_pos,
                                 float scale, uint16_t *o, uint8_t *q);
 
+/* ---- Q/K RMSNorm + NeoX RoPE over part of the head --------------------------
+ * The FP8-nope + BF16-rope KV pool that "perf: add fused norm + RoPE + uniform
+ * fp8 store for TRT-LLM DSv4 sparse attention" (SGLang PR 32975, review
+ * thread) names for the FlashMLA path.  The page does not give the split of a
+ * head; the reading taken: each head is [nope | rope] with the rotated part
+ * the LAST rope_dim elements.  Per head:
+ *   n   = RMSNorm of the whole head (as above), rounded to dt
+ *   o_i = n_i                                          for i < nope
+ *   with j = nope + i, i < rope_dim/2, c = cs[p][i], s = cs[p][rope_dim/2 + i]:
+ *   o_j              = dt(f32(f32(n_j * c) - f32(n_{j+rope_dim/2} * s)))
+ *   o_{j+rope_dim/2} = dt(f32(f32(n_{j+rope_dim/2} * c) + f32(n_j * s)))
+ * with nope = head_dim - rope_dim and cs a [max_pos, rope_dim] fp32 table
+ * (rope_dim/2 cos, then rope_dim/2 sin).  rope_dim == head_dim is the call
+ * above.  In the KV pool the nope part is stored as E4M3 (oracle_quant_fp8)
+ * and the rope part as the dtype values o. */
+void oracle_qk_rmsnorm_rope_partial(int dt, const uint16_t *src,
+                                    int64_t token_stride, int64_t n_tokens,
+                                    int n_heads, int head_dim, int rope_dim,
+                                    const uint16_t *w, float eps,
+                                    const int32_t *pos, const float *cos_sin,
+                                    int64_t max_pos, uint16_t *o);
+
 #ifdef __cplusplus
 }
 #endif
