@@ -114,6 +114,12 @@ struct BF16 {
         asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi_v), "f"(lo_v));
         return d;
     }
+    static __device__ __forceinline__ uint32_t mul2(uint32_t a, uint32_t b)
+    {
+        uint32_t d;
+        asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+        return d;
+    }
 };
 
 struct FP16 {
@@ -133,6 +139,12 @@ struct FP16 {
     {
         uint32_t d;
         asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi_v), "f"(lo_v));
+        return d;
+    }
+    static __device__ __forceinline__ uint32_t mul2(uint32_t a, uint32_t b)
+    {
+        uint32_t d;
+        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
         return d;
     }
 };
@@ -156,6 +168,20 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8])
     v.z = DT::pack(f[4], f[5]);
     v.w = DT::pack(f[6], f[7]);
     return v;
+}
+
+// ---------------------------------------------------------------- packed fp32
+// The product of two fp32 pairs, each half rounded once to nearest even, in a
+// form the compiler cannot fuse into a following addition.  Measured on
+// GB300: a packed multiply feeding a packed add is contracted into one packed
+// FMA (a single rounding) whether written with the __fmul2_rn / __fadd2_rn
+// intrinsics or as PTX mul.rn.f32x2 / add.rn.f32x2, and so is an FMA with a
+// constant -0 addend.  Here the product is an FMA whose addend nz is -0 known
+// only at run time (a kernel argument): RN(a b + -0) = RN(a b), signed zeros
+// included, and an FMA result cannot be merged into a later add.
+__device__ __forceinline__ float2 mul2_unfused(float2 a, float2 b, float nz)
+{
+    return __ffma2_rn(a, b, make_float2(nz, nz));
 }
 
 // ---------------------------------------------------------------- FP8 / FP4
@@ -295,40 +321,216 @@ __device__ __forceinline__ float2 div_by2(float2 a, const Divisor &d)
     return make_float2(copysignf(t.x, a.x), copysignf(t.y, a.y));
 }
 
-// silu(z) = z * sigmoid(z) in fp32.  With u = e^-|z| in (0, 1] (no
-// overflow for any z): sigmoid(z) = 1 / (1 + u) for z >= 0 and u / (1 + u)
-// for z < 0, the reciprocal from rcp.approx (its argument is in [1, 2]).
-// u = 2^t with t = -|z| log2(e) <= 0, split as 2^n * 2^f: n = rint(t), found
-// by adding 1.5 * 2^23 (which leaves n in the low bits of the sum), and the
-// fraction f = t - n formed with log2(e) in two parts, L1 + L2 (the range
+// ---------------------------------------------------------------- SiLU gate
+// The gate of the gated RMSNorm is dt(silu(z)) for a dtype value z, with
+// silu(z) = z / (1 + e^-z) rounded once to fp32 and then to the dtype.  It is
+// formed exactly: a fast fp32 estimate, a test of whether that estimate lies
+// within kSiluUlps fp32 ulps of a point where the dtype rounding changes, and
+// a double-precision evaluation for the elements where it does (a small
+// fraction of the dtype values; tests/cuda/silu_check.cu checks every one of
+// the 65,536 values of each dtype against the oracle's gate).
+
+// Bound on |bits(silu_fast(z)) - bits(RN32(silu(z)))| over every finite fp32
+// z >= -87 (the inputs silu_fast is used for), measured over all of them by
+// tests/cuda/silu_check.cu.
+constexpr int kSiluUlps = 8;
+
+// silu(z) from u = e^-|z| in (0, 1], which never overflows: sigmoid(z) is
+// 1 / (1 + u) for z >= 0 and u / (1 + u) for z < 0, and silu(z) =
+// max(z, z * u) / (1 + u) covers both (z * u <= z for z >= 0, >= z for
+// z < 0).  u = 2^t * e^d with t = RN(-|z| log2(e)) fed to the ex2.approx
+// instruction and d = -|z| - t ln 2, the part of the exponent that rounding t
+// dropped, taken in two FMAs with ln 2 split in two parts (the argument
 // reduction of Cody and Waite, "Software Manual for the Elementary
-// Functions", 1980): f = fma(-|z|, L2, fma(-|z|, L1, -n)), |f| <= 1/2 plus a
-// few ulps, so 2^f (in [0.7, 1.42]) comes from the ex2.approx instruction at
-// its full relative accuracy whatever |z|.  2^n is applied as 2^(n + 64),
-// built in the exponent field, then 2^-64; for z < 0 the product z * 2^f * r
-// is formed first and the power of two applied last, so that a result in
-// the subnormal range is rounded there once.  t is clamped at -152, below
-// which u rounds to 0.  Error against the correctly rounded silu: measured
-// over every fp32 input in tests/cuda/silu_check.cu.
-__device__ __forceinline__ float silu_f32(float z)
+// Functions", 1980); e^d is 1 + d to within d^2 / 2 < 2^-37.  The reciprocal
+// comes from rcp.approx on [1, 2].  For |z| above about 87, 2^t is below the
+// normal range and flushes to zero: silu(z) is then z for z > 0, and the
+// caller takes the exact path for z < -87.  |z| is clamped at 128 first, so
+// that t and d stay finite for the largest dtype values.
+__device__ __forceinline__ float silu_fast(float z)
 {
-    const float kL1 = 1.44269502162933349609375f;  // fp32 nearest log2(e)
-    const float kL2 = 1.9259629911266175e-8f;      // log2(e) - kL1
-    const float kRound = 12582912.0f;              // 1.5 * 2^23
-    const float na = -fabsf(z);
-    const float m = __fadd_rn(fmaxf(na * kL1, -152.0f), kRound);
-    const float n = __fsub_rn(m, kRound);  // rint(t), exactly
-    const float f = __fmaf_rn(na, kL2, __fmaf_rn(na, kL1, -n));
+    const float kLog2e = 1.44269502162933349609375f;     // RN(log2 e)
+    const float kLn2Hi = 0.693145751953125f;             // ln 2, 16 leading bits
+    const float kLn2Lo = 1.42860682030941723212e-6f;     // ln 2 - kLn2Hi
+    const float a = fminf(fabsf(z), 128.0f);  // keeps t and d finite for every finite z
+    const float t = __fmul_rn(-a, kLog2e);
     float p;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(p) : "f"(f));
-    // 2^(n + 64): n = bits(m) - bits(1.5 * 2^23), biased by 127
-    const float s64 = __int_as_float((__float_as_int(m) - 0x4B400000 + 64 + 127) << 23);
-    const float u = __fmul_rn(__fmul_rn(p, s64), 0x1p-64f);
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(p) : "f"(t));
+    const float d = __fmaf_rn(-t, kLn2Lo, __fmaf_rn(-t, kLn2Hi, -a));
+    const float u = __fmaf_rn(p, d, p);
     float r;
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(__fadd_rn(1.0f, u)));
-    const bool pos = z >= 0.0f;  // false for NaN, which stays NaN either way
-    const float a = __fmul_rn(__fmul_rn(z, pos ? 1.0f : p), r);
-    return __fmul_rn(__fmul_rn(a, pos ? 1.0f : s64), pos ? 1.0f : 0x1p-64f);
+    return __fmul_rn(fmaxf(z, __fmul_rn(z, u)), r);
+}
+
+// ---- double-float arithmetic: a value h + l held as two floats with
+// |l| <= ulp(h) / 2.  The error-free sum and product of two floats are
+// Dekker's ("A floating-point technique for extending the available
+// precision", Numer. Math. 18, 1971; also Knuth, TAOCP vol. 2, 4.2.2), the
+// product through one FMA.
+struct F2 {
+    float h, l;
+};
+
+// a + b exactly, for |a| >= |b| (or a == 0)
+__device__ __forceinline__ F2 fast_two_sum(float a, float b)
+{
+    const float s = __fadd_rn(a, b);
+    return F2{s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+
+// a + b exactly, any order of magnitude
+__device__ __forceinline__ F2 two_sum(float a, float b)
+{
+    const float s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    return F2{s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb))};
+}
+
+// a * b exactly (barring underflow)
+__device__ __forceinline__ F2 two_prod(float a, float b)
+{
+    const float p = __fmul_rn(a, b);
+    return F2{p, __fmaf_rn(a, b, -p)};
+}
+
+// silu(z) = z / (1 + e^-z) to a relative error of about 2^-43, in fp32
+// arithmetic, for -87 <= z <= 87 (the exact path of the gate; the double
+// precision units of this GPU run at a small fraction of the fp32 rate):
+//   e^-|z| = 2^-k e^-r, k = rint(|z| log2 e), r = |z| - k ln 2 with ln 2 in
+//     three parts (Cody and Waite; k ln2_1 and |z| - k ln2_1 are exact);
+//   e^-r by its Taylor series, the terms of degree 0..6 in double-float
+//     Horner steps (1/n! as double-floats) and those of degree 7..11, below
+//     2^-23 together, in fp32; the low part of -r enters as a factor 1 + s_l;
+//   silu = N / D with D = 1 + 2^-k e^-r and N = z (z >= 0) or z e^-r with the
+//     factor 2^-k applied to the quotient (z < 0), the quotient from one
+//     correction step of the fp32 quotient.
+// The result is the high part of the double-float quotient, i.e. the value
+// rounded once to fp32.
+__device__ __forceinline__ float silu_df(float z)
+{
+    if (z == 0.0f) return z;  // silu(+-0) = +-0
+    const float kLog2e = 1.44269502162933349609375f;  // RN(log2 e)
+    const float kLn2a = 0x1.62e4p-1f;                 // ln 2, 16 leading bits
+    const float kLn2b = 0x1.7f7d1cp-20f;              // RN(ln 2 - kLn2a)
+    const float kLn2c = 0x1.ef357ap-45f;              // RN(ln 2 - kLn2a - kLn2b)
+    const float a = fabsf(z);
+    const float k = rintf(__fmul_rn(a, kLog2e));
+    // r = a - k ln 2 as a double-float
+    const float r1 = __fmaf_rn(-k, kLn2a, a);  // exact
+    const F2 kb = two_prod(k, kLn2b);
+    F2 r = two_sum(r1, -kb.h);
+    r = fast_two_sum(r.h, __fsub_rn(r.l, __fmaf_rn(k, kLn2c, kb.l)));
+    const float sh = -r.h, sl = -r.l;  // e^-r = e^(sh + sl)
+    // Taylor tail, degrees 7..11, in fp32
+    float t = 0x1.ae6456p-26f;            // 1/11!
+    t = __fmaf_rn(t, sh, 0x1.27e4fcp-22f);  // 1/10!
+    t = __fmaf_rn(t, sh, 0x1.71de3ap-19f);  // 1/9!
+    t = __fmaf_rn(t, sh, 0x1.a01a02p-16f);  // 1/8!
+    t = __fmaf_rn(t, sh, 0x1.a01a02p-13f);  // 1/7!
+    // degrees 6 .. 0: acc = c_n + sh * acc in double-float; |sh * acc| < c_n
+    const float ch[7] = {1.0f, 1.0f, 0.5f, 0x1.555556p-3f, 0x1.555556p-5f, 0x1.111112p-7f,
+                         0x1.6c16c2p-10f};
+    const float cl[7] = {0.0f, 0.0f, 0.0f, -0x1.555556p-28f, -0x1.555556p-30f, -0x1.ddddep-32f,
+                         -0x1.27d27ep-35f};
+    F2 acc{t, 0.0f};
+#pragma unroll
+    for (int n = 6; n >= 0; --n) {
+        F2 pr = two_prod(sh, acc.h);
+        pr.l = __fmaf_rn(sh, acc.l, pr.l);
+        const F2 sm = fast_two_sum(ch[n], pr.h);
+        acc = fast_two_sum(sm.h, __fadd_rn(__fadd_rn(sm.l, pr.l), cl[n]));
+    }
+    // times (1 + sl)
+    const F2 e = fast_two_sum(acc.h, __fmaf_rn(acc.h, sl, acc.l));
+    // D = 1 + 2^-k e (k <= 126: the scale is a normal power of two)
+    const float scale = __int_as_float((127 - (int)k) << 23);
+    const float uh = __fmul_rn(e.h, scale), ul = __fmul_rn(e.l, scale);
+    const F2 d0 = fast_two_sum(1.0f, uh);
+    const F2 d = fast_two_sum(d0.h, __fadd_rn(d0.l, ul));
+    // N = z or z e
+    F2 nn{z, 0.0f};
+    if (z < 0.0f) {
+        nn = two_prod(z, e.h);
+        nn = fast_two_sum(nn.h, __fmaf_rn(z, e.l, nn.l));
+    }
+    // Q = N / D: the fp32 quotient, then one correction from the exact remainder
+    const float q1 = __fdiv_rn(nn.h, d.h);
+    const float rem = __fmaf_rn(-q1, d.l, __fadd_rn(__fmaf_rn(-q1, d.h, nn.h), nn.l));
+    const float q = __fadd_rn(q1, __fdiv_rn(rem, d.h));
+    return z < 0.0f ? __fmul_rn(q, scale) : q;
+}
+
+// The exact path of the gate: silu(z) rounded once to fp32.  z < -87 (where
+// the fp32 result can be subnormal) is evaluated in double precision with
+// CUDA's exp.
+static __device__ __noinline__ float silu_exact(float z)
+{
+    if (z < -87.0f) {
+        const double zd = z;
+        return (float)(zd / (1.0 + exp(-zd)));
+    }
+    return silu_df(z);
+}
+
+// True where the dtype rounding of an fp32 value within kSiluUlps ulps of v
+// could differ from that of v, or where silu_fast does not apply (z < -87).
+// bf16 keeps the upper 16 bits of the fp32 pattern, so the rounding changes
+// where the lower 16 bits pass 0x8000, for normal and subnormal values alike.
+// fp16 keeps 10 of the 23 fraction bits for |v| >= 2^-14 (the change at
+// 0x1000 of the lower 13 bits); smaller |v| (fp16 subnormals) always take the
+// exact path.
+template <typename DT>
+__device__ __forceinline__ bool silu_near_tie(float v, float z);
+
+template <>
+__device__ __forceinline__ bool silu_near_tie<BF16>(float v, float z)
+{
+    const uint32_t k = (__float_as_uint(v) << 16) + ((uint32_t)(kSiluUlps - 0x8000) << 16);
+    return k <= ((uint32_t)(2 * kSiluUlps) << 16) || z < -87.0f;
+}
+
+template <>
+__device__ __forceinline__ bool silu_near_tie<FP16>(float v, float z)
+{
+    const uint32_t k = (__float_as_uint(v) << 19) + ((uint32_t)(kSiluUlps - 0x1000) << 19);
+    return k <= ((uint32_t)(2 * kSiluUlps) << 19) || fabsf(v) < 0x1p-14f;
+}
+
+// The exact gates of the 8 dtype values of one 16-byte vector, as 8 dtype
+// values.  `valid` false (a vector past the end of the row, filled with
+// zeros) skips the exact path: silu(0) = 0 needs none.
+template <typename DT>
+__device__ __forceinline__ uint4 silu_gate8(const uint4 &zv, bool valid = true)
+{
+    float z[8], v[8];
+    unpack8<DT>(zv, z);
+    uint32_t slow = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        v[e] = silu_fast(z[e]);
+        slow |= (uint32_t)silu_near_tie<DT>(v[e], z[e]) << e;
+    }
+    if (valid && slow != 0) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            if (slow & (1u << e)) v[e] = silu_exact(z[e]);
+    }
+    return pack8<DT>(v);
+}
+
+// Elementwise product of two vectors of 8 dtype values, each rounded to
+// nearest even in the dtype.  The fp32 product of two bf16 (fp16) values is
+// exact, so this is the fp32 product rounded to the dtype.
+template <typename DT>
+__device__ __forceinline__ uint4 mul8(const uint4 &a, const uint4 &b)
+{
+    uint4 d;
+    d.x = DT::mul2(a.x, b.x);
+    d.y = DT::mul2(a.y, b.y);
+    d.z = DT::mul2(a.z, b.z);
+    d.w = DT::mul2(a.w, b.w);
+    return d;
 }
 
 // ---------------------------------------------------------------- reductions

@@ -158,20 +158,18 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
         float ss = 0.0f;
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
-            float a[8], b[8];
-            unpack8<DT>(xv[j], a);
-            unpack8<DT>(sv[j], b);
+            float a[8];
             if (is_gated<MODE>()) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) b[e] = silu_f32(b[e]);
-                unpack8<DT>(pack8<DT>(b), b);  // the gate rounded to the dtype
-#pragma unroll
-                for (int e = 0; e < 8; ++e) a[e] = __fmul_rn(a[e], b[e]);
+                const bool ok = row_ok && j * G + t < nvec;
+                sv[j] = mul8<DT>(xv[j], silu_gate8<DT>(sv[j], ok));  // the gate rounded to dt
             } else {
+                float b[8];
+                unpack8<DT>(xv[j], a);
+                unpack8<DT>(sv[j], b);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) a[e] = __fadd_rn(a[e], b[e]);
+                sv[j] = pack8<DT>(a);
             }
-            sv[j] = pack8<DT>(a);
             unpack8<DT>(sv[j], a);
 #pragma unroll
             for (int e = 0; e < 8; ++e) ss = __fmaf_rn(a[e], a[e], ss);  // squares are exact

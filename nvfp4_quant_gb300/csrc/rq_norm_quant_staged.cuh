@@ -67,20 +67,18 @@ __device__ __forceinline__ void staged_body(const NormQuantParams &p, uint4 *buf
         for (int i = 0; i < iters; ++i) {
             const int k = i * T + tid;
             if (k < nvec) {
-                float a[8], b[8];
-                unpack8<DT>(lds16(xs + k), a);
-                unpack8<DT>(lds16(rs + k), b);
+                float a[8];
+                uint4 sv;
                 if (is_gated<MODE>()) {  // g = dt(x * dt(silu(z)))
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) b[e] = silu_f32(b[e]);
-                    unpack8<DT>(pack8<DT>(b), b);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) a[e] = __fmul_rn(a[e], b[e]);
+                    sv = mul8<DT>(lds16(xs + k), silu_gate8<DT>(lds16(rs + k)));
                 } else {
+                    float b[8];
+                    unpack8<DT>(lds16(xs + k), a);
+                    unpack8<DT>(lds16(rs + k), b);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) a[e] = __fadd_rn(a[e], b[e]);
+                    sv = pack8<DT>(a);
                 }
-                const uint4 sv = pack8<DT>(a);
                 if (MODE != MODE_AMAX && !is_gated<MODE>())
                     st16(static_cast<uint8_t *>(p.res_out) + (row * H + (int64_t)k * 8) * 2, sv);
                 sts16(rs + k, sv);

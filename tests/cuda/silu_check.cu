@@ -1,20 +1,22 @@
-// silu_check.cu -- error of the library's fp32 SiLU (rq::silu_f32) against
-// the correctly rounded fp32 value of z / (1 + e^-z), taken from a double
-// precision evaluation, over every finite fp32 input z.  Prints the largest
-// error in fp32 ulps (of the reference) over normal results and the number
-// of those more than 1, 2 and 4 ulps off; for bf16 and fp16, how many of the
-// 65,536 dtype values of z give a different dtype-rounded SiLU; and the
-// largest error, in units of the smallest subnormal, over subnormal results.  Built and run by
-// tests/test_gpu_gated.py.
+// silu_check.cu -- checks of the library's SiLU gate (rq::silu_fast,
+// rq::silu_near_tie, rq::silu_gate8), built and run by tests/test_gpu_gated.py.
+//
+//  1. Over every finite fp32 z >= -87 (the inputs the fast path serves): the
+//     largest distance, counted in fp32 bit patterns (ulps), between
+//     silu_fast(z) and z / (1 + e^-z) evaluated in double precision and
+//     rounded once to fp32.  rq::kSiluUlps, the window of the near-tie test,
+//     must bound it.
+//  2. For bf16 and fp16, the gate dt(silu(z)) that silu_gate8 gives for every
+//     one of the 65,536 bit patterns z, written to the file named by argv[1]
+//     (65,536 bf16 gates, then 65,536 fp16 gates) for the test to compare with
+//     the oracle's, and how many of the patterns with |z| <= 8 took the exact
+//     path.
 #include <cstdio>
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
 
 #include "rq_device.cuh"
 
-__device__ unsigned long long g_over[3];
-__device__ unsigned int g_max_ulp, g_max_ulp_sub;
-__device__ unsigned int g_dt_diff[2];
+__device__ unsigned int g_max_bits;
+__device__ unsigned int g_slow[2];
 
 __device__ float ref_silu(float z)
 {
@@ -22,68 +24,83 @@ __device__ float ref_silu(float z)
     return (float)(d / (1.0 + exp(-d)));
 }
 
-__device__ float ulp_of(float v)
+// fp32 bit pattern as a signed position on the number line (+0 and -0 both 0)
+__device__ long long ordinal(float v)
 {
-    const float a = fabsf(v);
-    if (a < 0x1p-126f) return 0x1p-149f;
-    return __int_as_float(__float_as_int(a) & 0x7F800000) * 0x1p-23f;
+    const unsigned b = __float_as_uint(v);
+    const long long m = b & 0x7FFFFFFFu;
+    return (b >> 31) ? -m : m;
 }
 
-__global__ void check_all()
+__global__ void check_fast()
 {
     for (unsigned long long i = blockIdx.x * (unsigned long long)blockDim.x + threadIdx.x; i < (1ull << 32);
          i += (unsigned long long)gridDim.x * blockDim.x) {
         const float z = __uint_as_float((unsigned)i);
-        if (!isfinite(z)) continue;
-        const float ref = ref_silu(z), got = rq::silu_f32(z);
-        if (__float_as_uint(ref) == __float_as_uint(got)) continue;
-        const float err = fabsf(got - ref) / ulp_of(ref);
-        const unsigned e = err > 1e9f ? 1000000000u : (unsigned)ceilf(err);
-        if (fabsf(ref) < 0x1p-126f) {  // subnormal results: counted apart
-            atomicMax(&g_max_ulp_sub, e);
-            continue;
-        }
-        atomicMax(&g_max_ulp, e);
-        if (err > 1.0f) atomicAdd(&g_over[0], 1ull);
-        if (err > 2.0f) atomicAdd(&g_over[1], 1ull);
-        if (err > 4.0f) atomicAdd(&g_over[2], 1ull);
+        if (!isfinite(z) || z < -87.0f) continue;
+        const long long d = ordinal(rq::silu_fast(z)) - ordinal(ref_silu(z));
+        const unsigned long long a = d < 0 ? -d : d;
+        if (a) atomicMax(&g_max_bits, a > 0xFFFFFFFFull ? 0xFFFFFFFFu : (unsigned)a);
     }
 }
 
-__global__ void check_dtypes()
+// thread i: the 8 patterns 8i .. 8i + 7 of one dtype
+template <typename DT>
+__global__ void gates(unsigned short *out, int which)
 {
-    const unsigned b = blockIdx.x * blockDim.x + threadIdx.x;
-    if (b >= 65536u) return;
-    const unsigned short u = (unsigned short)b;
-    const float zb = __bfloat162float(__ushort_as_bfloat16(u));
-    if (isfinite(zb) &&
-        __bfloat16_as_ushort(__float2bfloat16_rn(ref_silu(zb))) !=
-            __bfloat16_as_ushort(__float2bfloat16_rn(rq::silu_f32(zb))))
-        atomicAdd(&g_dt_diff[0], 1u);
-    const float zh = __half2float(__ushort_as_half(u));
-    if (isfinite(zh) &&
-        __half_as_ushort(__float2half_rn(ref_silu(zh))) != __half_as_ushort(__float2half_rn(rq::silu_f32(zh))))
-        atomicAdd(&g_dt_diff[1], 1u);
+    const unsigned i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= 65536u / 8) return;
+    uint4 zv;
+    const unsigned b = 8 * i;
+    zv.x = b | ((b + 1) << 16);
+    zv.y = (b + 2) | ((b + 3) << 16);
+    zv.z = (b + 4) | ((b + 5) << 16);
+    zv.w = (b + 6) | ((b + 7) << 16);
+    const uint4 g = rq::silu_gate8<DT>(zv);
+    const unsigned w[4] = {g.x, g.y, g.z, g.w};
+    float z[8];
+    rq::unpack8<DT>(zv, z);
+    for (int e = 0; e < 8; ++e) {
+        out[b + e] = (unsigned short)(w[e / 2] >> (16 * (e & 1)));
+        if (fabsf(z[e]) <= 8.0f && rq::silu_near_tie<DT>(rq::silu_fast(z[e]), z[e]))
+            atomicAdd(&g_slow[which], 1u);
+    }
 }
 
-int main()
+int main(int argc, char **argv)
 {
+    if (argc < 2) {
+        std::printf("usage: silu_check <gates output file>\n");
+        return 2;
+    }
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0);
-    check_all<<<sms * 8, 256>>>();
-    check_dtypes<<<256, 256>>>();
+    unsigned short *d_out = nullptr;
+    if (cudaMalloc(&d_out, 2 * 65536 * sizeof(unsigned short)) != cudaSuccess) {
+        std::printf("error: cudaMalloc\n");
+        return 2;
+    }
+    check_fast<<<sms * 8, 256>>>();
+    gates<rq::BF16><<<32, 256>>>(d_out, 0);
+    gates<rq::FP16><<<32, 256>>>(d_out + 65536, 1);
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         std::printf("error %s\n", cudaGetErrorString(e));
         return 2;
     }
-    unsigned long long over[3];
-    unsigned int mx, mxs, dd[2];
-    cudaMemcpyFromSymbol(over, g_over, sizeof(over));
-    cudaMemcpyFromSymbol(&mx, g_max_ulp, sizeof(mx));
-    cudaMemcpyFromSymbol(&mxs, g_max_ulp_sub, sizeof(mxs));
-    cudaMemcpyFromSymbol(dd, g_dt_diff, sizeof(dd));
-    std::printf("silu max_ulp %u over1 %llu over2 %llu over4 %llu bf16_diff %u fp16_diff %u subnormal_max_ulp %u\n",
-                mx, over[0], over[1], over[2], dd[0], dd[1], mxs);
+    static unsigned short h[2 * 65536];
+    unsigned int mx = 0, slow[2] = {0, 0};
+    cudaMemcpy(h, d_out, sizeof(h), cudaMemcpyDeviceToHost);
+    cudaMemcpyFromSymbol(&mx, g_max_bits, sizeof(mx));
+    cudaMemcpyFromSymbol(slow, g_slow, sizeof(slow));
+    cudaFree(d_out);
+    FILE *f = std::fopen(argv[1], "wb");
+    if (!f || std::fwrite(h, sizeof(h), 1, f) != 1) {
+        std::printf("error: cannot write %s\n", argv[1]);
+        return 2;
+    }
+    std::fclose(f);
+    std::printf("silu max_bits %u window %d slow_bf16 %u slow_fp16 %u\n", mx, rq::kSiluUlps, slow[0],
+                slow[1]);
     return 0;
 }

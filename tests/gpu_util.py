@@ -83,8 +83,24 @@ def assert_nvfp4(p_gpu, sf_gpu, p_ref, sf_ref, y_ref, gs, dt):
     deq = e2m1[split_nibbles(p_gpu)] * np.repeat(sfv, 16, axis=1) / gs
     yv = pins.bits_to_f64(y_ref, dt)
     step = np.repeat(2.0 * sfv / gs, 16, axis=1)
-    # the bound needs a normal, unsaturated block scale (an oversized global
-    # scale saturates the E4M3 scale at 448 and then the E2M1 codes at 6)
+    # against y, the bound needs a normal, unsaturated block scale (an
+    # oversized global scale saturates the E4M3 scale at 448 and then the
+    # E2M1 codes at 6; a subnormal scale has too few bits to keep every
+    # element within one step of y, on either side)
     normal = np.repeat((sfv >= 2.0 ** -6) & (sfv < 448.0), 16, axis=1)
     err = np.abs(deq - yv)
     assert np.all(err[normal] <= step[normal] * (1 + 1e-6)), "dequant error above one block step"
+    # in those other blocks, against the oracle's own dequantised values:
+    # equal wherever the scale byte and the code are the oracle's, and
+    # otherwise within one step of the larger of the two block scales
+    sfr = e4m3[np.asarray(sf_ref)]
+    deq_ref = e2m1[split_nibbles(p_ref)] * np.repeat(sfr, 16, axis=1) / gs
+    same = (np.repeat(np.asarray(sf_gpu) == np.asarray(sf_ref), 16, axis=1) &
+            (split_nibbles(p_gpu) == split_nibbles(p_ref)))
+    other = ~normal
+    assert np.array_equal(deq[other & same], deq_ref[other & same]), \
+        "dequantised value differs from the oracle's with the same codes"
+    step2 = np.repeat(2.0 * np.maximum(sfv, sfr) / gs, 16, axis=1)
+    diff = np.abs(deq - deq_ref)
+    assert np.all(diff[other] <= step2[other] * (1 + 1e-6)), \
+        "dequantised value more than one step from the oracle's in a subnormal or saturated block"
