@@ -157,7 +157,9 @@ rq_status rq_qk_rmsnorm_rope_fp8(const void *q, const void *k,
  * Source: "perf: add fused norm + RoPE + uniform fp8 store for TRT-LLM DSv4
  * sparse attention" (SGLang PR 32975), review thread: the norm + RoPE kernel
  * with a store epilogue into a uniform FP8 KV pool.
- *   k_slots   [n_tokens] int64 (8-byte aligned); required when n_k_heads > 0
+ *   k_slots   [n_tokens] int64 (8-byte aligned); required when n_k_heads > 0.
+ *             Two tokens with the same slot both write that pool row; which
+ *             one lands last is unspecified, so slots should be distinct.
  */
 rq_status rq_qk_rmsnorm_rope_fp8_kv_store(
     const void *q, const void *k, int64_t q_token_stride,
@@ -169,6 +171,81 @@ rq_status rq_qk_rmsnorm_rope_fp8_kv_store(
     rq_stream_t stream);
 
 /*
+ * The Q/K call with K stored into a mixed KV-cache pool: FP8 for the part of
+ * each head that RoPE leaves alone ("nope") and the dtype for the rotated
+ * part ("rope").  Each head of 128 elements is read as [nope | rope] with the
+ * rotated part its LAST rope_dim elements:
+ *   n   = dt(RMSNorm(x) * w) over the whole head, as in the other Q/K calls;
+ *   NeoX RoPE on the last rope_dim elements only, pairs (j, j + rope_dim/2)
+ *   with j = 128 - rope_dim + i, i < rope_dim/2, angles cos_sin_cache[pos][i]
+ *   and cos_sin_cache[pos][rope_dim/2 + i]; the first 128 - rope_dim
+ *   elements pass unchanged (o = n);
+ *   Q: out = E4M3(o / q_scale) for all 128 elements, dense in q_out;
+ *   K: pool row k_slots[t], per head 128 + rope_dim bytes: the E4M3 codes
+ *      E4M3(o / k_scale) of the first 128 - rope_dim elements, then the last
+ *      rope_dim elements o as dtype values (2 bytes each, little-endian).
+ * Source: "perf: add fused norm + RoPE + uniform fp8 store for TRT-LLM DSv4
+ * sparse attention" (SGLang PR 32975), review thread: the FlashMLA
+ * counterpart's fused store into an "fp8 nope + bf16 rope" KV pool.  The
+ * page does not give the split of a head; the one above is a reading (the
+ * rotated part last, one per-tensor scale for the FP8 part).
+ *   rope_dim       16, 32, 64 or 128 (else RQ_ERR_UNSUPPORTED)
+ *   cos_sin_cache  [max_pos, rope_dim] fp32: rope_dim/2 cos, then rope_dim/2 sin
+ *   k_pool         [num_slots, n_k_heads, 128 + rope_dim] bytes (16-byte
+ *                  aligned); a slot outside [0, num_slots) stores nothing
+ *   k_slots        [n_tokens] int64 (8-byte aligned); required when
+ *                  n_k_heads > 0.  Two tokens with the same slot both write
+ *                  that row; which one lands last is unspecified.
+ *   other arguments as in rq_qk_rmsnorm_rope_fp8.
+ */
+rq_status rq_qk_rmsnorm_rope_fp8_kv_store_mixed(
+    const void *q, const void *k, int64_t q_token_stride,
+    int64_t k_token_stride, int64_t n_tokens, int n_q_heads, int n_k_heads,
+    int head_dim, int rope_dim, const void *q_weight, const void *k_weight,
+    float eps, const int32_t *positions, const float *cos_sin_cache,
+    int64_t max_pos, const float *d_q_scale, const float *d_k_scale,
+    uint8_t *q_out, uint8_t *k_pool, const int64_t *k_slots, int64_t num_slots,
+    rq_dtype dt, rq_stream_t stream);
+
+/*
+ * Q/K calibration: *d_q_amax = max |o| over every element of Q and *d_k_amax
+ * = max |o| over K, o the dtype-rounded output of the Q/K RMSNorm + RoPE (the
+ * values rq_qk_rmsnorm_rope_fp8 quantises).  Nothing else is written.  The
+ * call clears both on `stream` first; they may be the same address, which
+ * then receives one maximum over Q and K.  A side with no heads leaves its
+ * pointer untouched (it may be NULL).
+ * Source: the per-tensor scales of the pages are absolute maxima of the
+ * tensor they scale ("Add AutoDeploy NVFP4 RMSNorm quant fusion", Changes:
+ * reference module with input-scale calibration); for Q and K that tensor is
+ * the rotated output, one scale each.
+ */
+rq_status rq_qk_rmsnorm_rope_amax(const void *q, const void *k,
+                                  int64_t q_token_stride,
+                                  int64_t k_token_stride, int64_t n_tokens,
+                                  int n_q_heads, int n_k_heads, int head_dim,
+                                  const void *q_weight, const void *k_weight,
+                                  float eps, const int32_t *positions,
+                                  const float *cos_sin_cache, int64_t max_pos,
+                                  float *d_q_amax, float *d_k_amax,
+                                  rq_dtype dt, rq_stream_t stream);
+
+/*
+ * The Q/K call with dynamic per-tensor scales: the amax pass above
+ * accumulates into d_q_scale_out / d_k_scale_out, which are turned in place
+ * into the dequant scales amax / 448 (1 for a zero maximum), and the fused
+ * pass of rq_qk_rmsnorm_rope_fp8 then reads them.  No workspace.  The two
+ * outputs may be the same address (one scale for Q and K).
+ * Source: as rq_qk_rmsnorm_rope_amax.
+ */
+rq_status rq_qk_rmsnorm_rope_fp8_dynamic(
+    const void *q, const void *k, int64_t q_token_stride,
+    int64_t k_token_stride, int64_t n_tokens, int n_q_heads, int n_k_heads,
+    int head_dim, const void *q_weight, const void *k_weight, float eps,
+    const int32_t *positions, const float *cos_sin_cache, int64_t max_pos,
+    float *d_q_scale_out, float *d_k_scale_out, uint8_t *q_out, uint8_t *k_out,
+    rq_dtype dt, rq_stream_t stream);
+
+/*
  * Gated RMSNorm + NVFP4: the NVFP4 call with the residual add replaced by a
  * SiLU gate applied before the norm, and nothing written back:
  *   g_i = dt(x_i * dt(silu(z_i))),  silu(z) = z / (1 + e^-z)
@@ -177,11 +254,8 @@ rq_status rq_qk_rmsnorm_rope_fp8_kv_store(
  * Source: "Add AutoDeploy NVFP4 RMSNorm quant fusion", Changes: the fused
  * gated RMSNorm + NVFP4 op.  The page does not give the gating formula; the
  * one above is the separated sequence such an op replaces (gate, then the
- * norm over the whole row).  The kernel's fp32 SiLU is within 5 ulp of the
- * correctly rounded value (measured over every fp32 input), so where that
- * value lies next to a dtype rounding boundary, dt(silu(z)) can be one dtype
- * step from the correctly rounded one (1 of the 65,536 bf16 values, 1 of the
- * fp16 values).
+ * norm over the whole row).  dt(silu(z)) is exact: silu(z) rounded once to
+ * fp32, then to the dtype, for every finite dtype value z.
  *   x, z          [rows, hidden] dt, read
  *   norm_out      [rows, hidden] dt, written with y; may be NULL
  *   other arguments as in rq_add_rmsnorm_nvfp4; no output may overlap an

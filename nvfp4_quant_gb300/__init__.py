@@ -34,6 +34,14 @@ SIGNATURES = {
     "rq_qk_rmsnorm_rope_fp8_kv_store": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp,
                                                _vp, _f32, _vp, _vp, _i64, _vp, _vp, _vp, _vp,
                                                _vp, _i64, _int, _vp]),
+    "rq_qk_rmsnorm_rope_fp8_kv_store_mixed": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _int, _int,
+                                                     _int, _vp, _vp, _f32, _vp, _vp, _i64, _vp,
+                                                     _vp, _vp, _vp, _vp, _i64, _int, _vp]),
+    "rq_qk_rmsnorm_rope_amax": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp, _vp,
+                                       _f32, _vp, _vp, _i64, _vp, _vp, _int, _vp]),
+    "rq_qk_rmsnorm_rope_fp8_dynamic": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp,
+                                              _vp, _f32, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _int,
+                                              _vp]),
     "rq_add_rmsnorm_amax": (_int, [_vp, _vp, _vp, _f32, _vp, _i64, _i64, _int, _vp]),
     "rq_add_rmsnorm_fp8_per_token": (_int, [_vp, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _i64, _i64,
                                             _int, _vp]),
@@ -277,15 +285,19 @@ def _heads(t):
     return t.shape[0], t.shape[1], t.stride(0)
 
 
-def _qk_buffers(ref, hq, hk, positions, cos_sin_cache, q_out, k_out):
-    """Sizes of the Q/K call's side inputs and dense outputs (k_out None: pool)."""
+def _qk_buffers(ref, hq, hk, positions, cos_sin_cache, q_out, k_out, rope_dim=None, outs=True):
+    """Sizes of the Q/K call's side inputs and dense outputs (k_out None: pool;
+    outs False: a call without code outputs)."""
     t, d = ref.shape[0], ref.shape[2]
     if t == 0:
         return
     if positions is None or positions.numel() < t:
         raise ValueError("positions must hold one int32 per token")
-    if cos_sin_cache is None or cos_sin_cache.dim() != 2 or cos_sin_cache.shape[1] != d:
-        raise ValueError("cos_sin_cache must be a [max_pos, head_dim] float32 tensor")
+    cols = d if rope_dim is None else rope_dim
+    if cos_sin_cache is None or cos_sin_cache.dim() != 2 or cos_sin_cache.shape[1] != cols:
+        raise ValueError("cos_sin_cache must be a [max_pos, %d] float32 tensor" % cols)
+    if not outs:
+        return
     if hq > 0:
         _out(q_out, t * hq * d, "q_out")
     if hk > 0 and k_out is not None:
@@ -331,6 +343,72 @@ def rq_qk_rmsnorm_rope_fp8_kv_store(q, k, q_weight, k_weight, eps, positions, co
         _ptr(k_weight), float(eps), _ptr(positions), _ptr(cos_sin_cache), cos_sin_cache.shape[0],
         _ptr(q_scale), _ptr(k_scale), _ptr(q_out), _ptr(k_pool), _ptr(k_slots),
         0 if k_pool is None else k_pool.shape[0], _dt(ref), _stream(stream)))
+
+
+def _qk_pair(q, k):
+    tq, hq, sq = _heads(q)
+    tk, hk, sk = _heads(k)
+    ref = q if q is not None else k
+    if q is not None and k is not None and (tq != tk or q.dtype != k.dtype):
+        raise ValueError("q and k must have the same token count and dtype")
+    return ref, hq, sq, hk, sk
+
+
+def rq_qk_rmsnorm_rope_fp8_kv_store_mixed(q, k, q_weight, k_weight, eps, positions,
+                                          cos_sin_cache, q_scale, k_scale, q_out, k_pool, k_slots,
+                                          rope_dim, stream=None):
+    """Q/K RMSNorm + NeoX RoPE on the last rope_dim elements of each head; Q's
+    FP8 codes dense, K into a mixed KV pool (include/rq.h): k_pool uint8
+    [num_slots, n_k_heads, head_dim + rope_dim] (E4M3 of the first head_dim -
+    rope_dim elements, then rope_dim dtype values); cos_sin_cache float32
+    [max_pos, rope_dim]; k_slots int64 [n_tokens]."""
+    ref, hq, sq, hk, sk = _qk_pair(q, k)
+    _qk_buffers(ref, hq, hk, positions, cos_sin_cache, q_out, None, rope_dim)
+    if hk > 0 and ref.shape[0] > 0:
+        row = ref.shape[2] + rope_dim
+        if k_pool is None or k_pool.dim() != 3 or k_pool.shape[1:] != (hk, row) \
+                or not k_pool.is_contiguous():
+            raise ValueError("k_pool must be a contiguous [num_slots, n_k_heads, %d] tensor" % row)
+        if k_slots is None or k_slots.dtype != torch.int64 or k_slots.numel() < ref.shape[0]:
+            raise ValueError("k_slots must hold one int64 slot per token")
+    _check(lib().rq_qk_rmsnorm_rope_fp8_kv_store_mixed(
+        _ptr(q), _ptr(k), sq, sk, ref.shape[0], hq, hk, ref.shape[2], int(rope_dim),
+        _ptr(q_weight), _ptr(k_weight), float(eps), _ptr(positions), _ptr(cos_sin_cache),
+        cos_sin_cache.shape[0], _ptr(q_scale), _ptr(k_scale), _ptr(q_out), _ptr(k_pool),
+        _ptr(k_slots), 0 if k_pool is None else k_pool.shape[0], _dt(ref), _stream(stream)))
+
+
+def rq_qk_rmsnorm_rope_amax(q, k, q_weight, k_weight, eps, positions, cos_sin_cache, q_amax,
+                            k_amax, stream=None):
+    """q_amax[0] / k_amax[0] = max |o| over Q / K, o the dtype-rounded output of
+    the Q/K RMSNorm + RoPE (include/rq.h); they may be the same tensor."""
+    ref, hq, sq, hk, sk = _qk_pair(q, k)
+    _qk_buffers(ref, hq, hk, positions, cos_sin_cache, None, None, outs=False)
+    if hq > 0:
+        _out(q_amax, 4, "q_amax")
+    if hk > 0:
+        _out(k_amax, 4, "k_amax")
+    _check(lib().rq_qk_rmsnorm_rope_amax(
+        _ptr(q), _ptr(k), sq, sk, ref.shape[0], hq, hk, ref.shape[2], _ptr(q_weight),
+        _ptr(k_weight), float(eps), _ptr(positions), _ptr(cos_sin_cache), cos_sin_cache.shape[0],
+        _ptr(q_amax), _ptr(k_amax), _dt(ref), _stream(stream)))
+
+
+def rq_qk_rmsnorm_rope_fp8_dynamic(q, k, q_weight, k_weight, eps, positions, cos_sin_cache,
+                                   q_scale_out, k_scale_out, q_out, k_out, stream=None):
+    """The Q/K call with per-tensor scales amax(o) / 448 computed on the device
+    (include/rq.h); q_scale_out / k_scale_out: 1-element float32, written."""
+    ref, hq, sq, hk, sk = _qk_pair(q, k)
+    _qk_buffers(ref, hq, hk, positions, cos_sin_cache, q_out, k_out)
+    if hq > 0:
+        _out(q_scale_out, 4, "q_scale_out")
+    if hk > 0:
+        _out(k_scale_out, 4, "k_scale_out")
+    _check(lib().rq_qk_rmsnorm_rope_fp8_dynamic(
+        _ptr(q), _ptr(k), sq, sk, ref.shape[0], hq, hk, ref.shape[2], _ptr(q_weight),
+        _ptr(k_weight), float(eps), _ptr(positions), _ptr(cos_sin_cache), cos_sin_cache.shape[0],
+        _ptr(q_scale_out), _ptr(k_scale_out), _ptr(q_out), _ptr(k_out), _dt(ref),
+        _stream(stream)))
 
 
 def rq_nvfp4_packed_bytes(rows, hidden):

@@ -371,22 +371,36 @@ rq_status rq_add_rmsnorm_nvfp4_dynamic_swizzled(const void *x, const void *resid
 
 }  // extern "C"
 
-static rq_status qk_call(const void *q, const void *k, int64_t q_token_stride,
-                         int64_t k_token_stride, int64_t n_tokens, int n_q_heads, int n_k_heads,
-                         int head_dim, const void *q_weight, const void *k_weight, float eps,
-                         const int32_t *positions, const float *cos_sin_cache, int64_t max_pos,
-                         const float *d_q_scale, const float *d_k_scale, uint8_t *q_out,
-                         uint8_t *k_out, const int64_t *k_slots, int64_t num_slots, rq_dtype dt,
-                         rq_stream_t stream)
+namespace {
+
+// What a Q/K entry point asks of the kernel beyond the common arguments.
+struct QKCall {
+    int mode = rq::QK_STORE;
+    int rope_dim = RQ_QK_HEAD_DIM;       // QK_MIXED: the rotated tail of each head
+    const int64_t *k_slots = nullptr;    // KV-pool calls
+    int64_t num_slots = 0;
+    float *q_amax = nullptr, *k_amax = nullptr;  // QK_AMAX
+};
+
+// Argument checks of every Q/K call, then the launch.
+rq_status qk_call(const void *q, const void *k, int64_t q_token_stride, int64_t k_token_stride,
+                  int64_t n_tokens, int n_q_heads, int n_k_heads, int head_dim,
+                  const void *q_weight, const void *k_weight, float eps, const int32_t *positions,
+                  const float *cos_sin_cache, int64_t max_pos, const float *d_q_scale,
+                  const float *d_k_scale, uint8_t *q_out, uint8_t *k_out, const QKCall &c,
+                  rq_dtype dt, rq_stream_t stream)
 {
+    const bool amax = c.mode == rq::QK_AMAX, mixed = c.mode == rq::QK_MIXED;
     if (dt != RQ_BF16 && dt != RQ_FP16) return RQ_ERR_DTYPE;
     // limits that keep every byte extent below 2^63 and the head count in an int
     if (n_tokens < 0 || n_q_heads < 0 || n_k_heads < 0 || max_pos < 1 || n_tokens > (int64_t)1 << 36 ||
         n_q_heads > RQ_QK_MAX_HEADS || n_k_heads > RQ_QK_MAX_HEADS || max_pos > (int64_t)1 << 40 ||
         q_token_stride > (int64_t)1 << 40 || k_token_stride > (int64_t)1 << 40 ||
-        (k_slots && num_slots > (int64_t)1 << 40))
+        (c.k_slots && c.num_slots > (int64_t)1 << 40))
         return RQ_ERR_SHAPE;
     if (head_dim != RQ_QK_HEAD_DIM) return RQ_ERR_UNSUPPORTED;
+    if (mixed && c.rope_dim != 16 && c.rope_dim != 32 && c.rope_dim != 64 && c.rope_dim != 128)
+        return RQ_ERR_UNSUPPORTED;
     if (n_tokens == 0 || (n_q_heads == 0 && n_k_heads == 0)) return RQ_OK;
     const bool has_q = n_q_heads > 0, has_k = n_k_heads > 0;
     if (has_q && (q_token_stride < (int64_t)n_q_heads * head_dim || q_token_stride % 8 != 0))
@@ -394,29 +408,44 @@ static rq_status qk_call(const void *q, const void *k, int64_t q_token_stride,
     if (has_k && (k_token_stride < (int64_t)n_k_heads * head_dim || k_token_stride % 8 != 0))
         return k_token_stride % 8 != 0 ? RQ_ERR_MISALIGNED : RQ_ERR_SHAPE;
     if (!positions || !cos_sin_cache) return RQ_ERR_NULL;
-    if (has_q && (!q || !q_weight || !d_q_scale || !q_out)) return RQ_ERR_NULL;
-    if (has_k && (!k || !k_weight || !d_k_scale || !k_out)) return RQ_ERR_NULL;
-    if (k_slots && has_k && num_slots < 0) return RQ_ERR_SHAPE;
+    if (has_q && (!q || !q_weight || (!amax && (!d_q_scale || !q_out)) || (amax && !c.q_amax)))
+        return RQ_ERR_NULL;
+    if (has_k && (!k || !k_weight || (!amax && (!d_k_scale || !k_out)) || (amax && !c.k_amax)))
+        return RQ_ERR_NULL;
+    if (c.k_slots && has_k && c.num_slots < 0) return RQ_ERR_SHAPE;
     if (!aligned16(cos_sin_cache) || !aligned4(positions) ||
-        (k_slots && (reinterpret_cast<uintptr_t>(k_slots) & 7u)))
+        (c.k_slots && (reinterpret_cast<uintptr_t>(c.k_slots) & 7u)))
         return RQ_ERR_MISALIGNED;
-    if (has_q && (!aligned16(q) || !aligned16(q_weight) || !aligned16(q_out) || !aligned4(d_q_scale)))
+    if (has_q && (!aligned16(q) || !aligned16(q_weight) ||
+                  (!amax && (!aligned16(q_out) || !aligned4(d_q_scale))) ||
+                  (amax && !aligned4(c.q_amax))))
         return RQ_ERR_MISALIGNED;
-    if (has_k && (!aligned16(k) || !aligned16(k_weight) || !aligned16(k_out) || !aligned4(d_k_scale)))
+    if (has_k && (!aligned16(k) || !aligned16(k_weight) ||
+                  (!amax && (!aligned16(k_out) || !aligned4(d_k_scale))) ||
+                  (amax && !aligned4(c.k_amax))))
         return RQ_ERR_MISALIGNED;
     // input extents: the last token's heads end before (T-1)*stride + H*D
-    const int64_t qin = has_q && n_tokens > 0 ? ((n_tokens - 1) * q_token_stride + (int64_t)n_q_heads * head_dim) * 2 : 0;
-    const int64_t kin = has_k && n_tokens > 0 ? ((n_tokens - 1) * k_token_stride + (int64_t)n_k_heads * head_dim) * 2 : 0;
-    const int64_t k_rows = k_slots ? num_slots : n_tokens;
+    const int64_t qin = has_q ? ((n_tokens - 1) * q_token_stride + (int64_t)n_q_heads * head_dim) * 2 : 0;
+    const int64_t kin = has_k ? ((n_tokens - 1) * k_token_stride + (int64_t)n_k_heads * head_dim) * 2 : 0;
+    const int64_t table_cols = mixed ? c.rope_dim : head_dim;
+    const int64_t k_rows = c.k_slots ? c.num_slots : n_tokens;
+    const int64_t k_head_bytes = mixed ? head_dim + c.rope_dim : head_dim;
     const Span ins[] = {span(has_q ? q : nullptr, qin), span(has_k ? k : nullptr, kin),
                         span(has_q ? q_weight : nullptr, head_dim * 2),
                         span(has_k ? k_weight : nullptr, head_dim * 2), span(positions, n_tokens * 4),
-                        span(cos_sin_cache, max_pos * head_dim * 4),
-                        span(has_q ? d_q_scale : nullptr, 4), span(has_k ? d_k_scale : nullptr, 4),
-                        span(has_k ? k_slots : nullptr, n_tokens * 8)};
-    const Span outs[] = {span(has_q ? q_out : nullptr, n_tokens * n_q_heads * (int64_t)head_dim),
-                         span(has_k ? k_out : nullptr, k_rows * n_k_heads * (int64_t)head_dim)};
-    if (bad_alias(outs, 2, ins, 9)) return RQ_ERR_ALIAS;
+                        span(cos_sin_cache, max_pos * table_cols * 4),
+                        span(has_q && !amax ? d_q_scale : nullptr, 4),
+                        span(has_k && !amax ? d_k_scale : nullptr, 4),
+                        span(has_k ? c.k_slots : nullptr, n_tokens * 8)};
+    if (amax) {
+        // the two maxima may share one address (one maximum over Q and K)
+        const Span qa = span(has_q ? c.q_amax : nullptr, 4), ka = span(has_k ? c.k_amax : nullptr, 4);
+        if (bad_alias(&qa, 1, ins, 9) || bad_alias(&ka, 1, ins, 9)) return RQ_ERR_ALIAS;
+    } else {
+        const Span outs[] = {span(has_q ? q_out : nullptr, n_tokens * n_q_heads * (int64_t)head_dim),
+                             span(has_k ? k_out : nullptr, k_rows * n_k_heads * k_head_bytes)};
+        if (bad_alias(outs, 2, ins, 9)) return RQ_ERR_ALIAS;
+    }
 
     rq::QKParams p;
     p.q = q;
@@ -436,13 +465,33 @@ static rq_status qk_call(const void *q, const void *k, int64_t q_token_stride,
     p.k_scale = d_k_scale;
     p.q_out = q_out;
     p.k_out = k_out;
-    p.k_slots = has_k ? k_slots : nullptr;
-    p.num_slots = num_slots;
+    p.k_slots = has_k ? c.k_slots : nullptr;
+    p.num_slots = c.num_slots;
+    p.rope_dim = mixed ? c.rope_dim : head_dim;
+    p.q_amax = c.q_amax;
+    p.k_amax = c.k_amax;
+    p.nz = -0.0f;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = dt == RQ_BF16 ? rq::launch_qk_rmsnorm_rope_fp8<rq::BF16>(p, s)
-                                  : rq::launch_qk_rmsnorm_rope_fp8<rq::FP16>(p, s);
+    if (amax) {
+        cudaError_t e = cudaSuccess;
+        if (has_q) e = cudaMemsetAsync(c.q_amax, 0, sizeof(float), s);
+        if (e == cudaSuccess && has_k) e = cudaMemsetAsync(c.k_amax, 0, sizeof(float), s);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    cudaError_t e;
+    if (c.mode == rq::QK_AMAX)
+        e = dt == RQ_BF16 ? rq::launch_qk_rmsnorm_rope<rq::BF16, rq::QK_AMAX>(p, s)
+                          : rq::launch_qk_rmsnorm_rope<rq::FP16, rq::QK_AMAX>(p, s);
+    else if (c.mode == rq::QK_MIXED)
+        e = dt == RQ_BF16 ? rq::launch_qk_rmsnorm_rope<rq::BF16, rq::QK_MIXED>(p, s)
+                          : rq::launch_qk_rmsnorm_rope<rq::FP16, rq::QK_MIXED>(p, s);
+    else
+        e = dt == RQ_BF16 ? rq::launch_qk_rmsnorm_rope<rq::BF16, rq::QK_STORE>(p, s)
+                          : rq::launch_qk_rmsnorm_rope<rq::FP16, rq::QK_STORE>(p, s);
     return cuda_status(e);
 }
+
+}  // namespace
 
 extern "C" {
 
@@ -456,7 +505,7 @@ rq_status rq_qk_rmsnorm_rope_fp8(const void *q, const void *k, int64_t q_token_s
 {
     return qk_call(q, k, q_token_stride, k_token_stride, n_tokens, n_q_heads, n_k_heads, head_dim,
                    q_weight, k_weight, eps, positions, cos_sin_cache, max_pos, d_q_scale, d_k_scale,
-                   q_out, k_out, nullptr, 0, dt, stream);
+                   q_out, k_out, QKCall{}, dt, stream);
 }
 
 rq_status rq_qk_rmsnorm_rope_fp8_kv_store(const void *q, const void *k, int64_t q_token_stride,
@@ -470,9 +519,85 @@ rq_status rq_qk_rmsnorm_rope_fp8_kv_store(const void *q, const void *k, int64_t 
                                           int64_t num_slots, rq_dtype dt, rq_stream_t stream)
 {
     if (n_k_heads > 0 && n_tokens > 0 && !k_slots) return RQ_ERR_NULL;
+    QKCall c;
+    c.k_slots = k_slots;
+    c.num_slots = num_slots;
     return qk_call(q, k, q_token_stride, k_token_stride, n_tokens, n_q_heads, n_k_heads, head_dim,
                    q_weight, k_weight, eps, positions, cos_sin_cache, max_pos, d_q_scale, d_k_scale,
-                   q_out, k_pool, k_slots, num_slots, dt, stream);
+                   q_out, k_pool, c, dt, stream);
+}
+
+rq_status rq_qk_rmsnorm_rope_fp8_kv_store_mixed(
+    const void *q, const void *k, int64_t q_token_stride, int64_t k_token_stride, int64_t n_tokens,
+    int n_q_heads, int n_k_heads, int head_dim, int rope_dim, const void *q_weight,
+    const void *k_weight, float eps, const int32_t *positions, const float *cos_sin_cache,
+    int64_t max_pos, const float *d_q_scale, const float *d_k_scale, uint8_t *q_out,
+    uint8_t *k_pool, const int64_t *k_slots, int64_t num_slots, rq_dtype dt, rq_stream_t stream)
+{
+    if (n_k_heads > 0 && n_tokens > 0 && !k_slots) return RQ_ERR_NULL;
+    QKCall c;
+    c.mode = rq::QK_MIXED;
+    c.rope_dim = rope_dim;
+    c.k_slots = k_slots;
+    c.num_slots = num_slots;
+    return qk_call(q, k, q_token_stride, k_token_stride, n_tokens, n_q_heads, n_k_heads, head_dim,
+                   q_weight, k_weight, eps, positions, cos_sin_cache, max_pos, d_q_scale, d_k_scale,
+                   q_out, k_pool, c, dt, stream);
+}
+
+rq_status rq_qk_rmsnorm_rope_amax(const void *q, const void *k, int64_t q_token_stride,
+                                  int64_t k_token_stride, int64_t n_tokens, int n_q_heads,
+                                  int n_k_heads, int head_dim, const void *q_weight,
+                                  const void *k_weight, float eps, const int32_t *positions,
+                                  const float *cos_sin_cache, int64_t max_pos, float *d_q_amax,
+                                  float *d_k_amax, rq_dtype dt, rq_stream_t stream)
+{
+    QKCall c;
+    c.mode = rq::QK_AMAX;
+    c.q_amax = d_q_amax;
+    c.k_amax = d_k_amax;
+    rq_status st = qk_call(q, k, q_token_stride, k_token_stride, n_tokens, n_q_heads, n_k_heads,
+                           head_dim, q_weight, k_weight, eps, positions, cos_sin_cache, max_pos,
+                           nullptr, nullptr, nullptr, nullptr, c, dt, stream);
+    if (st != RQ_OK || (n_tokens > 0 && (n_q_heads > 0 || n_k_heads > 0))) return st;
+    // an empty call still clears the maxima it was given
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (n_q_heads > 0 && d_q_amax) {
+        if (!aligned4(d_q_amax)) return RQ_ERR_MISALIGNED;
+        st = cuda_status(cudaMemsetAsync(d_q_amax, 0, sizeof(float), s));
+    }
+    if (st == RQ_OK && n_k_heads > 0 && d_k_amax) {
+        if (!aligned4(d_k_amax)) return RQ_ERR_MISALIGNED;
+        st = cuda_status(cudaMemsetAsync(d_k_amax, 0, sizeof(float), s));
+    }
+    return st;
+}
+
+rq_status rq_qk_rmsnorm_rope_fp8_dynamic(const void *q, const void *k, int64_t q_token_stride,
+                                         int64_t k_token_stride, int64_t n_tokens, int n_q_heads,
+                                         int n_k_heads, int head_dim, const void *q_weight,
+                                         const void *k_weight, float eps,
+                                         const int32_t *positions, const float *cos_sin_cache,
+                                         int64_t max_pos, float *d_q_scale_out,
+                                         float *d_k_scale_out, uint8_t *q_out, uint8_t *k_out,
+                                         rq_dtype dt, rq_stream_t stream)
+{
+    // the maxima accumulate in the caller's scale outputs, which the fused
+    // pass then reads: no workspace
+    rq_status st = rq_qk_rmsnorm_rope_amax(q, k, q_token_stride, k_token_stride, n_tokens,
+                                           n_q_heads, n_k_heads, head_dim, q_weight, k_weight, eps,
+                                           positions, cos_sin_cache, max_pos, d_q_scale_out,
+                                           d_k_scale_out, dt, stream);
+    if (st != RQ_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (n_q_heads > 0 && d_q_scale_out)
+        st = cuda_status(rq::launch_scale_from_amax(d_q_scale_out, d_q_scale_out, 0, 1, s));
+    if (st == RQ_OK && n_k_heads > 0 && d_k_scale_out && d_k_scale_out != d_q_scale_out)
+        st = cuda_status(rq::launch_scale_from_amax(d_k_scale_out, d_k_scale_out, 0, 1, s));
+    if (st != RQ_OK || n_tokens == 0) return st;
+    return qk_call(q, k, q_token_stride, k_token_stride, n_tokens, n_q_heads, n_k_heads, head_dim,
+                   q_weight, k_weight, eps, positions, cos_sin_cache, max_pos, d_q_scale_out,
+                   d_k_scale_out, q_out, k_out, QKCall{}, dt, stream);
 }
 
 size_t rq_nvfp4_packed_bytes(int64_t rows, int64_t hidden)

@@ -48,7 +48,18 @@ struct QKParams {
     uint8_t *k_out;
     const int64_t *k_slots;  // null: K dense [T, Hk, D]; else K goes to pool row k_slots[t]
     int64_t num_slots;       // rows of the K pool
+    int rope_dim;            // rotated elements at the end of each head (QK_MIXED; else D)
+    float *q_amax;           // QK_AMAX outputs (may be the same address)
+    float *k_amax;
+    float nz;                // -0.0f, passed at run time (see mul2_unfused)
 };
+
+// What the Q/K kernel writes.  QK_STORE: FP8 codes of Q and K (K dense or to
+// pool rows by slot).  QK_AMAX: nothing but max |o| over Q and over K.
+// QK_MIXED: the RoPE on the last rope_dim elements of each head only; Q's FP8
+// codes dense, K to pool rows by slot as [E4M3 of the first D - rope_dim
+// elements | the last rope_dim elements as dtype values].
+enum QKMode { QK_STORE = 0, QK_AMAX = 1, QK_MIXED = 2 };
 
 // MODE_NVFP4 writes the block scales row-major [rows, H/16]; MODE_NVFP4_SWZ
 // writes them in the 128 x 4-tile layout of block-scaled GEMMs (sf_offset).
@@ -90,8 +101,8 @@ int device_sms(int dev);
 template <typename DT, int MODE>
 cudaError_t launch_add_rmsnorm(const NormQuantParams &p, cudaStream_t stream);
 
-template <typename DT>
-cudaError_t launch_qk_rmsnorm_rope_fp8(const QKParams &p, cudaStream_t stream);
+template <typename DT, int QMODE>
+cudaError_t launch_qk_rmsnorm_rope(const QKParams &p, cudaStream_t stream);
 
 // out = amax / 448 (nvfp4 == 0) or 2688 / amax (nvfp4 == 1); with
 // zero_to_one, a zero amax gives 1.  out may equal amax.

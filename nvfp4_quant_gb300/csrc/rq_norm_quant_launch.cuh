@@ -43,14 +43,13 @@ static cudaError_t launch_cfg(const NormQuantParams &p, cudaStream_t stream)
 }
 
 // Long rows through shared memory: 4 * hidden bytes of dynamic shared memory
-// per CTA; the resident-CTA count is cached per device for the last row length.
+// per CTA; the resident-CTA count is cached per device for the last row
+// length, the pair (shared memory bytes, CTAs per SM) in one 64-bit atomic so
+// that concurrent callers never pair one length's count with another's.
 template <typename DT, int MODE>
 static cudaError_t launch_staged(const NormQuantParams &p, cudaStream_t stream)
 {
-    struct Occ {
-        std::atomic<int> smem{0}, per_sm{0};
-    };
-    static Occ occ[kMaxDevices];
+    static std::atomic<uint64_t> occ[kMaxDevices];
     static std::atomic<int> attr_set[kMaxDevices];
     auto kern = add_rmsnorm_quant_staged_kernel<DT, MODE>;
     int dev = 0;
@@ -64,14 +63,13 @@ static cudaError_t launch_staged(const NormQuantParams &p, cudaStream_t stream)
         if (e != cudaSuccess) return e;
         attr_set[d].store(1, std::memory_order_relaxed);
     }
-    int per_sm = occ[d].smem.load(std::memory_order_relaxed) == smem
-                     ? occ[d].per_sm.load(std::memory_order_relaxed) : 0;
+    const uint64_t cached = occ[d].load(std::memory_order_relaxed);
+    int per_sm = (uint32_t)(cached >> 32) == (uint32_t)smem ? (int)(uint32_t)cached : 0;
     if (per_sm <= 0) {
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kStagedThreads, smem) !=
                 cudaSuccess || per_sm < 1)
             per_sm = 1;
-        occ[d].per_sm.store(per_sm, std::memory_order_relaxed);
-        occ[d].smem.store(smem, std::memory_order_relaxed);
+        occ[d].store(((uint64_t)(uint32_t)smem << 32) | (uint32_t)per_sm, std::memory_order_relaxed);
     }
     const int64_t full = (int64_t)device_sms(dev) * per_sm;
     const int grid = (int)(p.rows < full ? p.rows : full);

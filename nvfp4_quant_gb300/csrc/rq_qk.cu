@@ -33,13 +33,25 @@ constexpr int kQKBlock = 128;
 constexpr int kHeadDim = 128;
 constexpr int kPairs = 4;  // head pairs per step: 8 heads, 4 loads in flight per lane
 
-template <typename DT, bool kFast>
-__device__ __forceinline__ void qk_body(const QKParams &p)
+// QMODE (QKMode): QK_STORE and QK_MIXED write codes; QK_AMAX only reduces
+// max |o| per side into *p.q_amax / *p.k_amax (one atomic per CTA each).
+// QK_MIXED rotates the last rope_dim = R elements of each head only (lanes
+// 16 - R / 8 .. 15; the pair partner of lane l is l ^ (R / 16)) and sends K's
+// codes to pool rows of D + R bytes per head: the FP8 codes of the first
+// D - R elements, then the last R elements as dtype values.
+template <typename DT, bool kFast, int QMODE>
+__device__ __forceinline__ void qk_body(const QKParams &p, float (*red)[2])
 {
     const int lane16 = threadIdx.x & 15;
     const int half = (threadIdx.x >> 4) & 1;            // even or odd heads
-    const bool upper = lane16 >= 8;                     // holds elements 64..127
-    const int rot = (lane16 & 7) * 8;                   // first frequency of this lane
+    // rotation geometry: the partner lane (xor), whether this lane holds the
+    // upper half of its pairs, the first frequency, and (QK_MIXED) whether
+    // the lane's elements are rotated at all
+    const int R = QMODE == QK_MIXED ? p.rope_dim : kHeadDim;
+    const int xr = R >> 4;
+    const bool rotated = QMODE != QK_MIXED || lane16 >= 16 - (R >> 3);
+    const bool upper = (lane16 & xr) != 0;
+    const int rot = (lane16 & (xr - 1)) * 8;
     const int heads = p.hq + p.hk;
     const int64_t warp0 = ((int64_t)blockIdx.x * kQKBlock + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * kQKBlock) >> 5;
@@ -48,8 +60,9 @@ __device__ __forceinline__ void qk_body(const QKParams &p)
                               : make_uint4(0, 0, 0, 0);
     const uint4 kw = p.hk > 0 ? ld_keep16(static_cast<const uint8_t *>(p.kw) + lane16 * 16)
                               : make_uint4(0, 0, 0, 0);
-    const Divisor by_q(p.hq > 0 ? ld_f32(p.q_scale) : 1.0f);
-    const Divisor by_k(p.hk > 0 ? ld_f32(p.k_scale) : 1.0f);
+    const Divisor by_q(QMODE != QK_AMAX && p.hq > 0 ? ld_f32(p.q_scale) : 1.0f);
+    const Divisor by_k(QMODE != QK_AMAX && p.hk > 0 ? ld_f32(p.k_scale) : 1.0f);
+    float amax_q = 0.0f, amax_k = 0.0f;  // QK_AMAX
 
     const int groups = (heads + 2 * kPairs - 1) / (2 * kPairs);  // units per token
     // unit = tok * groups + g, stepped by nwarps = step_tok * groups + step_g
@@ -62,15 +75,21 @@ __device__ __forceinline__ void qk_body(const QKParams &p)
         const int h0 = g * 2 * kPairs;
         int pos = ld_s32(p.pos + tok);
         pos = pos < 0 ? 0 : (pos >= p.max_pos ? (int)(p.max_pos - 1) : pos);
-        const uint8_t *cs = reinterpret_cast<const uint8_t *>(p.cos_sin + (int64_t)pos * kHeadDim);
-        const uint4 c0 = ld_keep16(cs + rot * 4), c1 = ld_keep16(cs + rot * 4 + 16);
-        const uint4 s0 = ld_keep16(cs + (64 + rot) * 4), s1 = ld_keep16(cs + (64 + rot) * 4 + 16);
+        const uint8_t *cs = reinterpret_cast<const uint8_t *>(p.cos_sin + (int64_t)pos * R);
+        uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0, s0 = c0, s1 = c0;
+        if (rotated) {
+            c0 = ld_keep16(cs + rot * 4);
+            c1 = ld_keep16(cs + rot * 4 + 16);
+            s0 = ld_keep16(cs + ((R >> 1) + rot) * 4);
+            s1 = ld_keep16(cs + ((R >> 1) + rot) * 4 + 16);
+        }
         const float2 cp[4] = {make_float2(__uint_as_float(c0.x), __uint_as_float(c0.y)),
                               make_float2(__uint_as_float(c0.z), __uint_as_float(c0.w)),
                               make_float2(__uint_as_float(c1.x), __uint_as_float(c1.y)),
                               make_float2(__uint_as_float(c1.z), __uint_as_float(c1.w))};
-        // lanes holding elements 0..63 subtract m * sin, the others add it:
-        // fold that sign into the sine once per unit (RN(-x) = -RN(x))
+        // lanes holding the lower half of their pairs subtract m * sin, the
+        // others add it: fold that sign into the sine once per unit
+        // (RN(-x) = -RN(x))
         const uint32_t neg = upper ? 0u : 0x80000000u;
         const float2 sp[4] = {make_float2(__uint_as_float(s0.x ^ neg), __uint_as_float(s0.y ^ neg)),
                               make_float2(__uint_as_float(s0.z ^ neg), __uint_as_float(s0.w ^ neg)),
@@ -81,7 +100,7 @@ __device__ __forceinline__ void qk_body(const QKParams &p)
         // K destination row: the token itself, or its slot in the KV pool
         // (slots outside [0, num_slots) write nothing)
         int64_t krow = tok;
-        if (p.k_slots != nullptr) {
+        if (QMODE != QK_AMAX && p.k_slots != nullptr) {
             int64_t sl;
             asm volatile("ld.global.nc.s64 %0, [%1];" : "=l"(sl) : "l"(p.k_slots + tok));
             krow = (sl >= 0 && sl < p.num_slots) ? sl : -1;
@@ -130,22 +149,38 @@ __device__ __forceinline__ void qk_body(const QKParams &p)
                 const uint4 nv = pack8<DT>(n);
                 // the partner half of each rotation pair
                 uint4 pv;
-                pv.x = __shfl_xor_sync(0xFFFFFFFFu, nv.x, 8);
-                pv.y = __shfl_xor_sync(0xFFFFFFFFu, nv.y, 8);
-                pv.z = __shfl_xor_sync(0xFFFFFFFFu, nv.z, 8);
-                pv.w = __shfl_xor_sync(0xFFFFFFFFu, nv.w, 8);
+                pv.x = __shfl_xor_sync(0xFFFFFFFFu, nv.x, xr);
+                pv.y = __shfl_xor_sync(0xFFFFFFFFu, nv.y, xr);
+                pv.z = __shfl_xor_sync(0xFFFFFFFFu, nv.z, xr);
+                pv.w = __shfl_xor_sync(0xFFFFFFFFu, nv.w, xr);
                 unpack8<DT>(nv, n);
                 unpack8<DT>(pv, m);
                 float o[8];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
+                    // two products, each rounded, then their rounded sum (never
+                    // one FMA: see mul2_unfused)
                     const float2 oi =
-                        __fadd2_rn(__fmul2_rn(make_float2(n[2 * i], n[2 * i + 1]), cp[i]),
-                                   __fmul2_rn(make_float2(m[2 * i], m[2 * i + 1]), sp[i]));
+                        __fadd2_rn(mul2_unfused(make_float2(n[2 * i], n[2 * i + 1]), cp[i], p.nz),
+                                   mul2_unfused(make_float2(m[2 * i], m[2 * i + 1]), sp[i], p.nz));
                     o[2 * i] = oi.x;
                     o[2 * i + 1] = oi.y;
                 }
-                unpack8<DT>(pack8<DT>(o), o);  // FP8 from the dtype-rounded rotation
+                uint4 ov = pack8<DT>(o);
+                if (QMODE == QK_MIXED && !rotated) ov = nv;  // the unrotated part is n itself
+                unpack8<DT>(ov, o);  // FP8 from the dtype-rounded rotation
+                if (QMODE == QK_AMAX) {
+                    float a = 0.0f;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) a = fmaxf(a, fabsf(o[e]));
+                    if (h < heads) {
+                        if (is_q)
+                            amax_q = fmaxf(amax_q, a);
+                        else
+                            amax_k = fmaxf(amax_k, a);
+                    }
+                    continue;
+                }
                 const Divisor &by = is_q ? by_q : by_k;
                 float v[8];
 #pragma unroll
@@ -156,9 +191,19 @@ __device__ __forceinline__ void qk_body(const QKParams &p)
                 }
                 const uint2 code = e4m3x8(v);
                 if (h < heads && (is_q || krow >= 0)) {
-                    uint8_t *dst = is_q ? p.q_out + (tok * p.hq + h) * kHeadDim
-                                        : p.k_out + (krow * p.hk + (h - p.hq)) * kHeadDim;
-                    st8(dst + lane16 * 8, code.x, code.y);
+                    if (QMODE == QK_MIXED && !is_q) {
+                        // pool row: D + R bytes per head, codes then dtype values
+                        uint8_t *dst = p.k_out + (krow * p.hk + (h - p.hq)) * (int64_t)(kHeadDim + R);
+                        const int nope_lanes = 16 - (R >> 3);
+                        if (rotated)
+                            st16(dst + (kHeadDim - R) + (lane16 - nope_lanes) * 16, ov);
+                        else
+                            st8(dst + lane16 * 8, code.x, code.y);
+                    } else {
+                        uint8_t *dst = is_q ? p.q_out + (tok * p.hq + h) * kHeadDim
+                                            : p.k_out + (krow * p.hk + (h - p.hq)) * kHeadDim;
+                        st8(dst + lane16 * 8, code.x, code.y);
+                    }
                 }
             }
         }
@@ -169,25 +214,47 @@ __device__ __forceinline__ void qk_body(const QKParams &p)
             ++tok;
         }
     }
+
+    if (QMODE == QK_AMAX) {
+        // block maxima, then one atomic per CTA and side on the float's bits
+        // (non-negative floats order like their unsigned bits)
+        amax_q = group_max<32>(amax_q);
+        amax_k = group_max<32>(amax_k);
+        if ((threadIdx.x & 31) == 0) {
+            red[threadIdx.x >> 5][0] = amax_q;
+            red[threadIdx.x >> 5][1] = amax_k;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float aq = 0.0f, ak = 0.0f;
+            for (int i = 0; i < kQKBlock / 32; ++i) {
+                aq = fmaxf(aq, red[i][0]);
+                ak = fmaxf(ak, red[i][1]);
+            }
+            if (p.hq > 0) atomicMax(reinterpret_cast<unsigned int *>(p.q_amax), __float_as_uint(aq));
+            if (p.hk > 0) atomicMax(reinterpret_cast<unsigned int *>(p.k_amax), __float_as_uint(ak));
+        }
+    }
 }
 
-template <typename DT>
+template <typename DT, int QMODE>
 __global__ void __launch_bounds__(kQKBlock, 6)
-qk_rmsnorm_rope_fp8_kernel(const QKParams p)
+qk_rmsnorm_rope_kernel(const QKParams p)
 {
-    const bool fast = (p.hq == 0 || Divisor(ld_f32(p.q_scale)).fast) &&
-                      (p.hk == 0 || Divisor(ld_f32(p.k_scale)).fast);
+    __shared__ float red[kQKBlock / 32][2];
+    const bool fast = QMODE == QK_AMAX || ((p.hq == 0 || Divisor(ld_f32(p.q_scale)).fast) &&
+                                          (p.hk == 0 || Divisor(ld_f32(p.k_scale)).fast));
     if (fast)
-        qk_body<DT, true>(p);
+        qk_body<DT, true, QMODE>(p, red);
     else
-        qk_body<DT, false>(p);
+        qk_body<DT, false, QMODE>(p, red);
 }
 
-template <typename DT>
-cudaError_t launch_qk_rmsnorm_rope_fp8(const QKParams &p, cudaStream_t stream)
+template <typename DT, int QMODE>
+cudaError_t launch_qk_rmsnorm_rope(const QKParams &p, cudaStream_t stream)
 {
     static std::atomic<int> occ_cache[64];
-    auto kern = qk_rmsnorm_rope_fp8_kernel<DT>;
+    auto kern = qk_rmsnorm_rope_kernel<DT, QMODE>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -206,8 +273,12 @@ cudaError_t launch_qk_rmsnorm_rope_fp8(const QKParams &p, cudaStream_t stream)
     return cudaGetLastError();
 }
 
-template cudaError_t launch_qk_rmsnorm_rope_fp8<BF16>(const QKParams &, cudaStream_t);
-template cudaError_t launch_qk_rmsnorm_rope_fp8<FP16>(const QKParams &, cudaStream_t);
+#define RQ_QK_INSTANTIATE(DT)                                                                      \
+    template cudaError_t launch_qk_rmsnorm_rope<DT, QK_STORE>(const QKParams &, cudaStream_t);    \
+    template cudaError_t launch_qk_rmsnorm_rope<DT, QK_AMAX>(const QKParams &, cudaStream_t);     \
+    template cudaError_t launch_qk_rmsnorm_rope<DT, QK_MIXED>(const QKParams &, cudaStream_t);
+RQ_QK_INSTANTIATE(BF16)
+RQ_QK_INSTANTIATE(FP16)
 
 // ---- scales from a calibrated amax: one fp32 IEEE division each
 __global__ void scale_from_amax_kernel(const float *amax, float *out, int nvfp4, int zero_to_one)

@@ -237,3 +237,39 @@ def test_kv_store_rejections(L):
     assert f(ns=-1) == SHAPE
     assert f(pool=A["y"]) == ALIAS  # pool over the slot indices
     assert f(T=0, slots=None) == OK
+
+
+def test_kv_store_mixed_rejections(L):
+    f = lambda **kw: L.rq_qk_rmsnorm_rope_fp8_kv_store_mixed(
+        A["x"], A["k"], 16 * 128, 8 * 128, kw.get("T", 32), 16, kw.get("hk", 8), 128,
+        kw.get("rd", 64), A["w"], A["r"], 1e-6, A["pos"], A["cs"], 4096, A["qs"], A["ks"], A["qo"],
+        kw.get("pool", A["ko"]), kw.get("slots", A["y"]), kw.get("ns", 100), 0, None)
+    for rd in (0, 8, 48, 96, 256):
+        assert f(rd=rd) == UNSUP
+    assert f(slots=None) == NULL
+    assert f(slots=A["y"] + 4) == MISAL
+    assert f(pool=A["ko"] + 8) == MISAL
+    assert f(ns=-1) == SHAPE
+    # the pool rows are 8 heads x (128 + 64) bytes: one just below the slot
+    # indices reaches into them
+    assert f(pool=A["y"] - 100 * 8 * 192 + 16) == ALIAS
+    assert f(pool=A["y"] - 100 * 8 * 192) != ALIAS
+    assert f(T=0, slots=None) == OK
+
+
+def test_qk_amax_and_dynamic_rejections(L):
+    am = lambda **kw: L.rq_qk_rmsnorm_rope_amax(
+        kw.get("q", A["x"]), A["k"], 16 * 128, 8 * 128, 32, 16, kw.get("hk", 8), 128, A["w"],
+        A["r"], 1e-6, A["pos"], A["cs"], 4096, kw.get("qa", A["qs"]), kw.get("ka", A["ks"]),
+        kw.get("dt", 0), None)
+    assert am(qa=None) == NULL
+    assert am(ka=None) == NULL
+    assert am(qa=A["qs"] + 2) == MISAL
+    assert am(qa=A["x"] + 64) == ALIAS  # the maximum inside Q
+    assert am(dt=2) == DTYPE
+    dyn = lambda **kw: L.rq_qk_rmsnorm_rope_fp8_dynamic(
+        A["x"], A["k"], 16 * 128, 8 * 128, 32, 16, 8, 128, A["w"], A["r"], 1e-6, A["pos"], A["cs"],
+        4096, kw.get("qs", A["qs"]), kw.get("ks", A["ks"]), kw.get("qo", A["qo"]), A["ko"], 0, None)
+    assert dyn(qs=None) == NULL
+    assert dyn(ks=A["ks"] + 1) == MISAL
+    assert dyn(qs=A["cs"] + 16) == ALIAS
