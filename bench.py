@@ -63,6 +63,14 @@ def alg_bytes_qk(t, hq, hk, d):
     return t * (hq + hk) * d * (2 + 1) + t * d * 4 + t * 4 + 2 * d * 2 + 8
 
 
+def alg_bytes_qk_mixed(t, hq, hk, d, rope_dim):
+    # q, k read; Q codes; K pool rows of (d - rope_dim) codes + rope_dim dtype
+    # values; slots; one table row (rope_dim floats) and position per token;
+    # weights, scales
+    return (t * (hq + hk) * d * 2 + t * hq * d + t * hk * (d + rope_dim) + t * 8 +
+            t * (rope_dim * 4 + 4) + 2 * d * 2 + 8)
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -170,6 +178,7 @@ class Workload:
         self.w3, self.w5 = dev16(w3).cuda(), dev16(w5).cuda()
         self.qw4, self.kw4 = dev16(qw4).cuda(), dev16(kw4).cuda()
         self.cs4 = torch.from_numpy(cs4).cuda()
+        self.cs4_rope64 = torch.from_numpy(synth.rope_cos_sin(QK_T, 64, 1.0e6)).cuda()
         u8 = dict(dtype=torch.uint8, device="cuda")
         self.ro3 = torch.empty_like(d["r3"])
         self.q3 = torch.empty((FP8_ROWS, FP8_H), **u8)
@@ -191,15 +200,12 @@ class Workload:
         rq.rq_fp8_scale_from_amax(a3, self.s3)
         rq.rq_add_rmsnorm_amax(d["x5"], d["r5"], self.w5, EPS, a5)
         rq.rq_nvfp4_global_scale_from_amax(a5, self.gs5)
-        # Q/K: one uniform per-tensor scale each for Q and K, amax/448 of the
-        # per-head norm output (the caller's calibration choice; the rotation
-        # keeps each pair's norm, so a few rotated values may saturate at 448)
+        # Q/K: one per-tensor scale each for Q and K, amax(o)/448 of the
+        # rotated output o that the call quantises
         self.qs4, self.ks4 = f(), f()
         aq, ak = f(), f()
-        rq.rq_add_rmsnorm_amax(d["q4"].view(-1, QK_D), torch.zeros_like(d["q4"]).view(-1, QK_D),
-                               self.qw4, EPS, aq)
-        rq.rq_add_rmsnorm_amax(d["k4"].view(-1, QK_D), torch.zeros_like(d["k4"]).view(-1, QK_D),
-                               self.kw4, EPS, ak)
+        rq.rq_qk_rmsnorm_rope_amax(d["q4"], d["k4"], self.qw4, self.kw4, EPS, d["pos4"], self.cs4,
+                                   aq, ak)
         rq.rq_fp8_scale_from_amax(aq, self.qs4)
         rq.rq_fp8_scale_from_amax(ak, self.ks4)
         torch.cuda.synchronize()
@@ -232,6 +238,25 @@ KERNELS = [
      alg_bytes_nvfp4(NV_ROWS, NV_H)),
 ]
 STEP_BYTES = sum(k[3] for k in KERNELS)
+
+
+def step_config(ws=1):
+    """The workload of one step (the same for both arms)."""
+    return {
+        "workload": "fused norm+quant prologue step: add_rmsnorm_fp8 65536x1024 bf16 + "
+                    "qk_rmsnorm_rope_fp8 4096 tok x (16+8) heads x 128 bf16 + "
+                    "add_rmsnorm_nvfp4 16384x7168 bf16 with bf16 norm out",
+        "rows_per_step": ROWS_PER_STEP,
+        "row_note": "a Q/K row is one 128-element head of one token",
+        "io": "bf16 in; bf16 residual / norm out, E4M3 and packed E2M1 + E4M3 scales out; "
+              "every step computed in fp32",
+        "scales": "static, calibrated once before timing: FP8 amax(y)/448, NVFP4 2688/amax(y), "
+                  "Q and K amax(o)/448 each",
+        "alg_bytes_per_step": STEP_BYTES,
+        "l2": "no flush: each kernel's inputs were last touched > 1 GB of HBM traffic "
+              "earlier (L2 129 MB), residual written out of place so every step is identical",
+        "parallelism": "replicas" if ws > 1 else "single GPU",
+    }
 
 
 def run_ours(args):
@@ -306,20 +331,8 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic (seeded splitmix64 normals, rounded to bf16)",
-        "config": {
-            "workload": "fused norm+quant prologue step: add_rmsnorm_fp8 65536x1024 bf16 + "
-                        "qk_rmsnorm_rope_fp8 4096 tok x (16+8) heads x 128 bf16 + "
-                        "add_rmsnorm_nvfp4 16384x7168 bf16 with bf16 norm out",
-            "rows_per_step": ROWS_PER_STEP,
-            "row_note": "a Q/K row is one 128-element head of one token",
-            "io": "bf16 in; bf16 residual / norm out, E4M3 and packed E2M1 + E4M3 scales out; "
-                  "every step computed in fp32",
-            "alg_bytes_per_step": STEP_BYTES,
-            "step_gbs": round(STEP_BYTES / (ms_per_step / 1e3) / 1e9, 1),
-            "l2": "no flush: each kernel's inputs were last touched > 1 GB of HBM traffic "
-                  "earlier (L2 129 MB), residual written out of place so every step is identical",
-            "parallelism": "replicas" if ws > 1 else "single GPU",
-        },
+        "config": step_config(ws),
+        "step_gbs": round(STEP_BYTES / (ms_per_step / 1e3) / 1e9, 1),
         "kernels": kernels,
         "roofline": {"kernel": dname, "bound": "hbm", "achieved": dgbs, "peak": peak,
                      "unit": "GB/s", "frac": round(dgbs / peak, 4), "peak_kind": peak_kind,
@@ -332,11 +345,7 @@ def run_ours(args):
         "clocks": clk.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"], inputs = cpu_baseline(args.cpu_seconds)
-        n = host_threads()
-        spent, desc = oracle_step_threads(n, inputs)
-        line["cpu_baseline_threads"] = {"value": ROWS_PER_STEP / spent, "unit": "rows/s", "cores": n,
-                                        "kind": "oracle, row-parallel", "sample": desc}
+        line["cpu_baseline"], line["cpu_baseline_threads"] = cpu_baselines(args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -350,8 +359,10 @@ def measure_next_rows(wl, peak_kind_gbs, iters=50):
     prefill / large NVFP4 workloads, the large NVFP4 call with its block
     scales in the swizzled GEMM layout (same bytes: 16,384 rows and 7168
     columns need no padding), the gated RMSNorm + NVFP4 call on the same
-    rows (the residual as the gate), and the Q/K call storing K into a KV
-    pool of 8192 slots at shuffled slot indices."""
+    rows (the residual as the gate), the Q/K call storing K into a KV pool
+    of 8192 slots at shuffled slot indices (uniform FP8 rows, and mixed rows
+    of 64 FP8 codes + 64 bf16 rope values per head), and the Q/K call with
+    dynamic scales (amax pass + fused pass)."""
     rq, d = wl.rq, wl.d
     f = lambda: torch.zeros(1, dtype=torch.float32, device="cuda")
     row_scales = torch.empty(FP8_ROWS, dtype=torch.float32, device="cuda")
@@ -385,6 +396,21 @@ def measure_next_rows(wl, peak_kind_gbs, iters=50):
                   lambda: rq.rq_qk_rmsnorm_rope_fp8_kv_store(d["q4"], d["k4"], wl.qw4, wl.kw4, EPS,
                                                              d["pos4"], wl.cs4, wl.qs4, wl.ks4,
                                                              wl.qo4, pool, slots)))
+    # the mixed pool: K heads as 64 FP8 bytes + 64 bf16 values (rope_dim 64)
+    pool_mixed = torch.empty((n_slots, QK_HK, QK_D + 64), dtype=torch.uint8, device="cuda")
+    cases.append(("qk_rmsnorm_rope_fp8_kv_store_mixed_rope64", QK_T * (QK_HQ + QK_HK),
+                  alg_bytes_qk_mixed(QK_T, QK_HQ, QK_HK, QK_D, 64),
+                  lambda: rq.rq_qk_rmsnorm_rope_fp8_kv_store_mixed(
+                      d["q4"], d["k4"], wl.qw4, wl.kw4, EPS, d["pos4"], wl.cs4_rope64, wl.qs4,
+                      wl.ks4, wl.qo4, pool_mixed, slots, 64)))
+    # dynamic Q/K scales: an amax pass (reads Q, K and the table) then the fused pass
+    qs_dyn, ks_dyn = f(), f()
+    cases.append(("qk_rmsnorm_rope_fp8_dynamic", QK_T * (QK_HQ + QK_HK),
+                  alg_bytes_qk(QK_T, QK_HQ, QK_HK, QK_D) +
+                  QK_T * (QK_HQ + QK_HK) * QK_D * 2 + QK_T * (QK_D * 4 + 4) + 2 * QK_D * 2 + 8,
+                  lambda: rq.rq_qk_rmsnorm_rope_fp8_dynamic(d["q4"], d["k4"], wl.qw4, wl.kw4, EPS,
+                                                            d["pos4"], wl.cs4, qs_dyn, ks_dyn,
+                                                            wl.qo4, wl.ko4)))
     out = {}
     stream = torch.cuda.current_stream()
     for name, rows, nbytes, fn in cases:
@@ -630,71 +656,73 @@ def oracle_inputs(frac_rows):
             "qk": synth.qk_input(0, t4, QK_HQ, QK_HK, QK_D, "bf16")}
 
 
-def oracle_step_sample(frac_rows, inputs=None):
-    """Time the oracle on a sample of each call of the step; returns
-    (seconds per full step extrapolated by rows, seconds spent, sample
-    description, the inputs used)."""
-    import oracle as O
-    inputs = inputs or oracle_inputs(frac_rows)
-    x3, rr3, w3 = inputs["fp8"]
-    x5, rr5, w5 = inputs["nvfp4"]
-    q4, k4, qw4, kw4, pos4, cs4 = inputs["qk"]
-    r3, r5, t4 = x3.shape[0], x5.shape[0], q4.shape[0]
-    O.lib()
-    t = time.perf_counter()
-    O.add_rmsnorm_fp8("bf16", x3, rr3, w3, EPS, 0.01)
-    t_fp8 = time.perf_counter() - t
-    t = time.perf_counter()
-    O.qk_rmsnorm_rope_fp8("bf16", q4.reshape(-1), QK_HQ * QK_D, t4, QK_HQ, QK_D, qw4, EPS, pos4, cs4, 0.01)
-    O.qk_rmsnorm_rope_fp8("bf16", k4.reshape(-1), QK_HK * QK_D, t4, QK_HK, QK_D, kw4, EPS, pos4, cs4, 0.01)
-    t_qk = time.perf_counter() - t
-    t = time.perf_counter()
-    O.add_rmsnorm_nvfp4("bf16", x5, rr5, w5, EPS, 400.0)
-    t_nv = time.perf_counter() - t
-    full = t_fp8 * FP8_ROWS / r3 + t_qk * QK_T / t4 + t_nv * NV_ROWS / r5
-    desc = ("oracle (single-threaded C) on %d of %d FP8 rows, %d of %d Q/K tokens, %d of %d "
-            "NVFP4 rows; time scaled to a full step by rows" % (r3, FP8_ROWS, t4, QK_T, r5, NV_ROWS))
-    return full, t_fp8 + t_qk + t_nv, desc, inputs
+def _cuts(n, parts):
+    return [(i * n // parts, (i + 1) * n // parts) for i in range(parts)]
 
 
-def oracle_step_threads(n_threads, inputs=None):
-    """The same oracle, on one full step of inputs split by rows (tokens for
-    Q/K) over n_threads host threads.  The oracle is plain C called through
-    ctypes, which releases the GIL, so the slices run in parallel; nothing in
-    the oracle changes.  Returns (seconds per step, description)."""
+def oracle_scales(inputs, n_threads):
+    """The step's calibrated scales, computed by the oracle itself (untimed
+    set-up): FP8 amax(y)/448, NVFP4 2688/amax(y), Q and K amax(o)/448 each,
+    over the whole of each tensor, rows split over n_threads host threads."""
     import oracle as O
     from concurrent.futures import ThreadPoolExecutor
-    if inputs is None or inputs["fp8"][0].shape[0] != FP8_ROWS or inputs["nvfp4"][0].shape[0] != NV_ROWS \
-            or inputs["qk"][0].shape[0] != QK_T:
-        inputs = oracle_inputs(1.0)
     x3, rr3, w3 = inputs["fp8"]
     x5, rr5, w5 = inputs["nvfp4"]
     q4, k4, qw4, kw4, pos4, cs4 = inputs["qk"]
     O.lib()
 
-    def cuts(n):
-        return [(i * n // n_threads, (i + 1) * n // n_threads) for i in range(n_threads)]
+    def row_amax(x, r, w, a, b):
+        return O.amax("bf16", O.add_rmsnorm("bf16", x[a:b], r[a:b], w, EPS)[1])
 
-    def fp8(a, b):
-        O.add_rmsnorm_fp8("bf16", x3[a:b], rr3[a:b], w3, EPS, 0.01)
-
-    def qk(a, b):
-        O.qk_rmsnorm_rope_fp8("bf16", q4[a:b].reshape(-1), QK_HQ * QK_D, b - a, QK_HQ, QK_D, qw4, EPS,
-                              pos4[a:b], cs4, 0.01)
-        O.qk_rmsnorm_rope_fp8("bf16", k4[a:b].reshape(-1), QK_HK * QK_D, b - a, QK_HK, QK_D, kw4, EPS,
-                              pos4[a:b], cs4, 0.01)
-
-    def nv(a, b):
-        O.add_rmsnorm_nvfp4("bf16", x5[a:b], rr5[a:b], w5, EPS, 400.0)
+    def qk_amax(src, heads, w, a, b):
+        return O.amax("bf16", O.qk_rmsnorm_rope("bf16", src[a:b].reshape(-1), heads * QK_D, b - a,
+                                                heads, QK_D, w, EPS, pos4[a:b], cs4))
 
     with ThreadPoolExecutor(max_workers=n_threads) as ex:
+        a3 = max(ex.map(lambda c: row_amax(x3, rr3, w3, *c), _cuts(x3.shape[0], n_threads)))
+        a5 = max(ex.map(lambda c: row_amax(x5, rr5, w5, *c), _cuts(x5.shape[0], n_threads)))
+        aq = max(ex.map(lambda c: qk_amax(q4, QK_HQ, qw4, *c), _cuts(q4.shape[0], n_threads)))
+        ak = max(ex.map(lambda c: qk_amax(k4, QK_HK, kw4, *c), _cuts(k4.shape[0], n_threads)))
+    return {"s3": O.fp8_scale_from_amax(a3), "gs5": O.nvfp4_gs_from_amax(a5),
+            "qs4": O.fp8_scale_from_amax(aq), "ks4": O.fp8_scale_from_amax(ak)}
+
+
+def oracle_step(inputs, scales, n_threads):
+    """One pass of the unchanged oracle over the step's three calls (or a row
+    sample of them), rows (tokens for Q/K) split over n_threads host threads;
+    ctypes releases the GIL around the C calls, so the slices run in
+    parallel.  Returns (seconds, rows processed)."""
+    import oracle as O
+    from concurrent.futures import ThreadPoolExecutor
+    x3, rr3, w3 = inputs["fp8"]
+    x5, rr5, w5 = inputs["nvfp4"]
+    q4, k4, qw4, kw4, pos4, cs4 = inputs["qk"]
+    O.lib()
+
+    def fp8(a, b):
+        O.add_rmsnorm_fp8("bf16", x3[a:b], rr3[a:b], w3, EPS, scales["s3"])
+
+    def qk(a, b):
+        O.qk_rmsnorm_rope_fp8("bf16", q4[a:b].reshape(-1), QK_HQ * QK_D, b - a, QK_HQ, QK_D, qw4,
+                              EPS, pos4[a:b], cs4, scales["qs4"])
+        O.qk_rmsnorm_rope_fp8("bf16", k4[a:b].reshape(-1), QK_HK * QK_D, b - a, QK_HK, QK_D, kw4,
+                              EPS, pos4[a:b], cs4, scales["ks4"])
+
+    def nv(a, b):
+        O.add_rmsnorm_nvfp4("bf16", x5[a:b], rr5[a:b], w5, EPS, scales["gs5"])
+
+    jobs = ((fp8, x3.shape[0]), (qk, q4.shape[0]), (nv, x5.shape[0]))
+    rows = x3.shape[0] + q4.shape[0] * (QK_HQ + QK_HK) + x5.shape[0]
+    if n_threads == 1:
         t = time.perf_counter()
-        for fn, n in ((fp8, FP8_ROWS), (qk, QK_T), (nv, NV_ROWS)):
-            list(ex.map(lambda c: fn(*c), cuts(n)))
-        spent = time.perf_counter() - t
-    desc = ("the same oracle on one full step (%d FP8 rows, %d Q/K tokens, %d NVFP4 rows), rows "
-            "split over %d host threads" % (FP8_ROWS, QK_T, NV_ROWS, n_threads))
-    return spent, desc
+        for fn, n in jobs:
+            fn(0, n)
+        return time.perf_counter() - t, rows
+    with ThreadPoolExecutor(max_workers=n_threads) as ex:
+        t = time.perf_counter()
+        for fn, n in jobs:
+            list(ex.map(lambda c: fn(*c), _cuts(n, n_threads)))
+        return time.perf_counter() - t, rows
 
 
 def host_threads():
@@ -704,42 +732,65 @@ def host_threads():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(target_seconds):
-    """(the single-threaded baseline, the inputs it ran on)"""
-    # size the sample so the oracle runs about target_seconds
-    full, spent, _, _ = oracle_step_sample(1.0 / 256)
+def cpu_baselines(target_seconds):
+    """The oracle timed on this host at the step's own scales (computed by the
+    oracle): single-threaded on a row sample sized to about target_seconds
+    (a rate: rows processed / seconds), and on one full step with the rows
+    split over every host thread."""
+    n = host_threads()
+    full = oracle_inputs(1.0)
+    scales = oracle_scales(full, n)
+    threaded_s, rows_full = oracle_step(full, scales, n)
+    # size the single-threaded sample from a small probe
+    probe = oracle_inputs(1.0 / 256)
+    spent, _ = oracle_step(probe, scales, 1)
     frac = min(1.0, (1.0 / 256) * target_seconds / max(spent, 1e-3))
-    full, spent, desc, inputs = oracle_step_sample(frac)
-    return ({"value": ROWS_PER_STEP / full, "unit": "rows/s", "cores": 1, "kind": "oracle",
-             "sample": desc + " (%.1f s of CPU work)" % spent}, inputs)
+    sample = oracle_inputs(frac)
+    spent, rows = oracle_step(sample, scales, 1)
+    x3, x5, q4 = sample["fp8"][0], sample["nvfp4"][0], sample["qk"][0]
+    single = {"value": rows / spent, "unit": "rows/s", "cores": 1, "kind": "oracle",
+              "sample": "single-threaded C oracle on the first %d of %d FP8 rows, %d of %d Q/K "
+                        "tokens and %d of %d NVFP4 rows of the step, at the step's calibrated "
+                        "scales: %d rows in %.1f s" % (x3.shape[0], FP8_ROWS, q4.shape[0], QK_T,
+                                                       x5.shape[0], NV_ROWS, rows, spent)}
+    threads = {"value": rows_full / threaded_s, "unit": "rows/s", "cores": n,
+               "kind": "oracle, row-parallel",
+               "sample": "the same oracle on one full step (%d rows) at the step's calibrated "
+                         "scales, rows split over %d host threads: %.2f s" % (rows_full, n,
+                                                                             threaded_s)}
+    return single, threads
 
 
 def run_reference(args):
+    """The reference arm: the oracle (the pages hold no code to install),
+    unchanged, on the full step of the same workload, rows split over every
+    host thread; W untimed and K timed steps; no extrapolation."""
     ws, rank, _ = dist_env()
     if rank != 0:
         return
-    frac = args.ref_fraction
-    inputs = oracle_inputs(frac)
+    n = host_threads()
+    inputs = oracle_inputs(1.0)
+    scales = oracle_scales(inputs, n)
     for _ in range(args.warmup):
-        oracle_step_sample(frac, inputs)
-    fulls, spents = [], []
+        oracle_step(inputs, scales, n)
+    spent = []
+    rows = 0
     for _ in range(args.steps):
-        full, spent, desc, _ = oracle_step_sample(frac, inputs)
-        fulls.append(full)
-        spents.append(spent)
-    ms = statistics.mean(fulls) * 1e3
-    value = ROWS_PER_STEP / (ms / 1e3)
+        t, rows = oracle_step(inputs, scales, n)
+        spent.append(t)
+    ms = statistics.mean(spent) * 1e3
+    value = rows / (ms / 1e3)
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded splitmix64 normals)",
+        "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded splitmix64 normals, rounded to bf16)",
         "impl": "reference",
-        "config": {"workload": "fused norm+quant prologue step: add_rmsnorm_fp8 65536x1024 bf16 + "
-                               "qk_rmsnorm_rope_fp8 4096 tok x (16+8) heads x 128 bf16 + "
-                               "add_rmsnorm_nvfp4 16384x7168 bf16 with bf16 norm out",
-                   "rows_per_step": ROWS_PER_STEP},
-        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
-                         "sample": desc + " per step"},
+        "config": step_config(),
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": n, "kind": "oracle",
+                         "sample": "the whole step (%d rows) per step, the unchanged C oracle with "
+                                   "rows split over %d host threads, at the step's scales "
+                                   "calibrated by the oracle" % (rows, n)},
         "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -753,7 +804,6 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ref-fraction", type=float, default=1.0 / 128)
     args = ap.parse_args()
     if args.warmup < 3:
         print("bench: at least 3 warm-up steps are required", file=sys.stderr)
