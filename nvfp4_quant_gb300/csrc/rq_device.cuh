@@ -195,13 +195,31 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo_v, float hi_v)
     return d;
 }
 
+// Four fp32 -> four E4M3 bytes in one word, element a in the lowest byte.
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d)
+{
+    uint32_t r;
+    asm("{ .reg .b16 lo, hi;\n"
+        " cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n"
+        " cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n"
+        " mov.b32 %0, {lo, hi}; }"
+        : "=r"(r) : "f"(a), "f"(b), "f"(c), "f"(d));
+    return r;
+}
+
 // Eight fp32 -> eight E4M3 bytes, element 0 in the lowest byte of .x.
 __device__ __forceinline__ uint2 e4m3x8(const float (&v)[8])
 {
-    uint2 r;
-    r.x = e4m3x2(v[0], v[1]) | (e4m3x2(v[2], v[3]) << 16);
-    r.y = e4m3x2(v[4], v[5]) | (e4m3x2(v[6], v[7]) << 16);
-    return r;
+    return make_uint2(e4m3x4(v[0], v[1], v[2], v[3]), e4m3x4(v[4], v[5], v[6], v[7]));
+}
+
+// The sign bits of 8 dtype values (a 16-byte vector) placed on 8 E4M3 code
+// bytes: byte e of the result has bit 7 set where element e is negative.
+__device__ __forceinline__ uint2 sign_bytes8(const uint4 &v)
+{
+    // bytes 1 and 3 of each word hold the sign bits of its two elements at bit 7
+    return make_uint2(__byte_perm(v.x, v.y, 0x7531) & 0x80808080u,
+                      __byte_perm(v.z, v.w, 0x7531) & 0x80808080u);
 }
 
 // Eight fp32 -> eight E2M1 nibbles packed in 32 bits, element 0 in the
@@ -303,6 +321,22 @@ __device__ __forceinline__ float div_by(float a, const Divisor &d)
     return copysignf(fma_rn(r, d.y, q), a);
 }
 
+// |a| / b for two dividends with Blackwell's packed fp32 ops, rounded as the
+// IEEE quotient (the steps of div_by without the final copysign; callers put
+// the sign back on the encoded result).
+template <bool kFast>
+__device__ __forceinline__ float2 div_mag_by2(float2 a, const Divisor &d)
+{
+    if (!kFast) return make_float2(div_rn(fabsf(a.x), d.b), div_rn(fabsf(a.y), d.b));
+    float2 m;
+    asm("{ .reg .f32 t; abs.f32 t, %1; min.NaN.f32 %0, t, %2; }" : "=f"(m.x) : "f"(a.x), "f"(d.clamp));
+    asm("{ .reg .f32 t; abs.f32 t, %1; min.NaN.f32 %0, t, %2; }" : "=f"(m.y) : "f"(a.y), "f"(d.clamp));
+    const float2 y2 = make_float2(d.y, d.y);
+    const float2 q = __fmul2_rn(m, y2);
+    const float2 r = __ffma2_rn(q, make_float2(-d.b, -d.b), m);
+    return __ffma2_rn(r, y2, q);
+}
+
 // The same division for two dividends with Blackwell's packed fp32 ops: each
 // step is the same IEEE operation on both halves (fma(q, -b, m) equals
 // fma(-q, b, m) exactly, negation being exact), so every result is bit for
@@ -331,9 +365,10 @@ __device__ __forceinline__ float2 div_by2(float2 a, const Divisor &d)
 // the 65,536 values of each dtype against the oracle's gate).
 
 // Bound on |bits(silu_fast(z)) - bits(RN32(silu(z)))| over every finite fp32
-// z >= -87 (the inputs silu_fast is used for), measured over all of them by
-// tests/cuda/silu_check.cu.
-constexpr int kSiluUlps = 8;
+// z >= -87 (the inputs silu_fast is used for): 5, measured over all of them by
+// tests/cuda/silu_check.cu.  (The gate's exactness does not rest on it alone:
+// the same program checks the final gate of every dtype value.)
+constexpr int kSiluUlps = 5;
 
 // silu(z) from u = e^-|z| in (0, 1], which never overflows: sigmoid(z) is
 // 1 / (1 + u) for z >= 0 and u / (1 + u) for z < 0, and silu(z) =
@@ -394,18 +429,30 @@ __device__ __forceinline__ F2 two_prod(float a, float b)
     return F2{p, __fmaf_rn(a, b, -p)};
 }
 
+// x * y + c as a double-float, for a float x and double-floats y, c with
+// |x y| < |c.h| (the Taylor steps below); error about 2^-46 |c|.
+__device__ __forceinline__ F2 df_fma(float x, const F2 &y, const F2 &c)
+{
+    F2 pr = two_prod(x, y.h);
+    pr.l = __fmaf_rn(x, y.l, pr.l);
+    const F2 sm = fast_two_sum(c.h, pr.h);
+    return fast_two_sum(sm.h, __fadd_rn(__fadd_rn(sm.l, pr.l), c.l));
+}
+
 // silu(z) = z / (1 + e^-z) to a relative error of about 2^-43, in fp32
 // arithmetic, for -87 <= z <= 87 (the exact path of the gate; the double
 // precision units of this GPU run at a small fraction of the fp32 rate):
 //   e^-|z| = 2^-k e^-r, k = rint(|z| log2 e), r = |z| - k ln 2 with ln 2 in
 //     three parts (Cody and Waite; k ln2_1 and |z| - k ln2_1 are exact);
-//   e^-r by its Taylor series, the terms of degree 0..6 in double-float
-//     Horner steps (1/n! as double-floats) and those of degree 7..11, below
-//     2^-23 together, in fp32; the low part of -r enters as a factor 1 + s_l;
-//   silu = N / D with D = 1 + 2^-k e^-r and N = z (z >= 0) or z e^-r with the
-//     factor 2^-k applied to the quotient (z < 0), the quotient from one
-//     correction step of the fp32 quotient.
-// The result is the high part of the double-float quotient, i.e. the value
+//   e^s, s = -r, by its Taylor series: the terms of degree 0..7 as
+//     double-floats (1/n! as double-floats), grouped in pairs and combined
+//     with powers of s (Estrin's scheme, for a short chain of dependent
+//     steps), those of degree 8..11, below 2^-26 together, in fp32; the low
+//     part of s enters as a factor 1 + s_l;
+//   silu = N / D with D = 1 + 2^-k e^s and N = z (z >= 0) or z e^s with the
+//     factor 2^-k applied to the quotient (z < 0); the quotient from the
+//     reciprocal of D's high part and one correction from the remainder.
+// The result is the high part of the double-float quotient: the value
 // rounded once to fp32.
 __device__ __forceinline__ float silu_df(float z)
 {
@@ -421,26 +468,31 @@ __device__ __forceinline__ float silu_df(float z)
     const F2 kb = two_prod(k, kLn2b);
     F2 r = two_sum(r1, -kb.h);
     r = fast_two_sum(r.h, __fsub_rn(r.l, __fmaf_rn(k, kLn2c, kb.l)));
-    const float sh = -r.h, sl = -r.l;  // e^-r = e^(sh + sl)
-    // Taylor tail, degrees 7..11, in fp32
-    float t = 0x1.ae6456p-26f;            // 1/11!
-    t = __fmaf_rn(t, sh, 0x1.27e4fcp-22f);  // 1/10!
-    t = __fmaf_rn(t, sh, 0x1.71de3ap-19f);  // 1/9!
-    t = __fmaf_rn(t, sh, 0x1.a01a02p-16f);  // 1/8!
-    t = __fmaf_rn(t, sh, 0x1.a01a02p-13f);  // 1/7!
-    // degrees 6 .. 0: acc = c_n + sh * acc in double-float; |sh * acc| < c_n
-    const float ch[7] = {1.0f, 1.0f, 0.5f, 0x1.555556p-3f, 0x1.555556p-5f, 0x1.111112p-7f,
-                         0x1.6c16c2p-10f};
-    const float cl[7] = {0.0f, 0.0f, 0.0f, -0x1.555556p-28f, -0x1.555556p-30f, -0x1.ddddep-32f,
-                         -0x1.27d27ep-35f};
-    F2 acc{t, 0.0f};
-#pragma unroll
-    for (int n = 6; n >= 0; --n) {
-        F2 pr = two_prod(sh, acc.h);
-        pr.l = __fmaf_rn(sh, acc.l, pr.l);
-        const F2 sm = fast_two_sum(ch[n], pr.h);
-        acc = fast_two_sum(sm.h, __fadd_rn(__fadd_rn(sm.l, pr.l), cl[n]));
-    }
+    const float sh = -r.h, sl = -r.l;  // e^-r = e^(sh + sl), |sh| <= 0.35
+    // degrees 8..11 in fp32
+    float t = __fmaf_rn(sh, 0x1.ae6456p-26f, 0x1.27e4fcp-22f);  // 1/11!, 1/10!
+    t = __fmaf_rn(__fmul_rn(sh, sh), t, __fmaf_rn(sh, 0x1.71de3ap-19f, 0x1.a01a02p-16f));  // 1/9!, 1/8!
+    // pairs c_2j + c_2j+1 sh as double-floats
+    const F2 p0 = fast_two_sum(1.0f, sh);                                         // 1 + s
+    const F2 p1 = df_fma(sh, F2{0x1.555556p-3f, -0x1.555556p-28f}, F2{0.5f, 0.0f});  // 1/2 + s/6
+    const F2 p2 = df_fma(sh, F2{0x1.111112p-7f, -0x1.ddddep-32f},
+                         F2{0x1.555556p-5f, -0x1.555556p-30f});                  // 1/24 + s/120
+    // 1/720 + s/5040 + s^2 t
+    const F2 p3 = df_fma(sh, F2{0x1.a01a02p-13f, -0x1.7f97fap-39f},
+                         F2{0x1.6c16c2p-10f, __fmaf_rn(__fmul_rn(sh, sh), t, -0x1.27d27ep-35f)});
+    // s^2 as a double-float, then (p0 + s2 p1) + s2^2 (p2 + s2 p3)
+    const F2 s2 = two_prod(sh, sh);
+    auto df_mul_add = [](const F2 &x, const F2 &y, const F2 &c) {  // x * y + c, |x y| < |c|
+        F2 pr = two_prod(x.h, y.h);
+        pr.l = __fmaf_rn(x.h, y.l, __fmaf_rn(x.l, y.h, pr.l));
+        const F2 sm = fast_two_sum(c.h, pr.h);
+        return fast_two_sum(sm.h, __fadd_rn(__fadd_rn(sm.l, pr.l), c.l));
+    };
+    const F2 lo = df_mul_add(s2, p1, p0);
+    const F2 hi = df_mul_add(s2, p3, p2);
+    F2 s4 = two_prod(s2.h, s2.h);
+    s4.l = __fmaf_rn(2.0f * s2.h, s2.l, s4.l);
+    F2 acc = df_mul_add(s4, hi, lo);
     // times (1 + sl)
     const F2 e = fast_two_sum(acc.h, __fmaf_rn(acc.h, sl, acc.l));
     // D = 1 + 2^-k e (k <= 126: the scale is a normal power of two)
@@ -454,10 +506,13 @@ __device__ __forceinline__ float silu_df(float z)
         nn = two_prod(z, e.h);
         nn = fast_two_sum(nn.h, __fmaf_rn(z, e.l, nn.l));
     }
-    // Q = N / D: the fp32 quotient, then one correction from the exact remainder
-    const float q1 = __fdiv_rn(nn.h, d.h);
+    // Q = N / D: q1 from the reciprocal of d.h, then one correction from the
+    // remainder N - q1 D
+    float rc;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rc) : "f"(d.h));
+    const float q1 = __fmul_rn(nn.h, rc);
     const float rem = __fmaf_rn(-q1, d.l, __fadd_rn(__fmaf_rn(-q1, d.h, nn.h), nn.l));
-    const float q = __fadd_rn(q1, __fdiv_rn(rem, d.h));
+    const float q = __fadd_rn(q1, __fmul_rn(rem, rc));
     return z < 0.0f ? __fmul_rn(q, scale) : q;
 }
 

@@ -181,15 +181,20 @@ __device__ __forceinline__ void qk_body(const QKParams &p, float (*red)[2])
                     }
                     continue;
                 }
+                // codes of |o| / scale, then the signs of o on the code bytes
+                // (signed zeros included)
                 const Divisor &by = is_q ? by_q : by_k;
                 float v[8];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const float2 vi = div_by2<kFast>(make_float2(o[2 * i], o[2 * i + 1]), by);
+                    const float2 vi = div_mag_by2<kFast>(make_float2(o[2 * i], o[2 * i + 1]), by);
                     v[2 * i] = vi.x;
                     v[2 * i + 1] = vi.y;
                 }
-                const uint2 code = e4m3x8(v);
+                uint2 code = e4m3x8(v);
+                const uint2 sgn = sign_bytes8(ov);
+                code.x |= sgn.x;
+                code.y |= sgn.y;
                 if (h < heads && (is_q || krow >= 0)) {
                     if (QMODE == QK_MIXED && !is_q) {
                         // pool row: D + R bytes per head, codes then dtype values
