@@ -301,9 +301,16 @@ def run_ours(args):
     value = ROWS_PER_STEP * ws * args.steps / (total_ms / 1e3)
 
     # ---- end to end through the public API with host buffers
-    e2e = run_e2e(args, wl, ws)
-    next_rows = measure_next_rows(wl, peak_kind_gbs=peaks()[0])
-    small = measure_small_configs(wl)
+    if args.profile:
+        # the command of the committed ncu captures: the step as above, then
+        # one launch of each call beyond the step, nothing else
+        measure_next_rows(wl, peak_kind_gbs=peaks()[0], iters=1, evict=False)
+        torch.cuda.synchronize()
+        e2e = next_rows = small = None
+    else:
+        e2e = run_e2e(args, wl, ws)
+        next_rows = measure_next_rows(wl, peak_kind_gbs=peaks()[0])
+        small = measure_small_configs(wl)
 
     peak, peak_kind = peaks()
     kernels = {}
@@ -344,7 +351,7 @@ def run_ours(args):
         "gpu_launches": len(calls) * args.steps,
         "clocks": clk.summary(),
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and not args.profile:
         line["cpu_baseline"], line["cpu_baseline_threads"] = cpu_baselines(args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -353,7 +360,7 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def measure_next_rows(wl, peak_kind_gbs, iters=50):
+def measure_next_rows(wl, peak_kind_gbs, iters=50, evict=True):
     """Calls beyond the step, timed on their own: per-token FP8 on the prefill
     workload, per-tensor dynamic FP8 / NVFP4 (amax pass + fused pass) on the
     prefill / large NVFP4 workloads, the large NVFP4 call with its block
@@ -414,7 +421,7 @@ def measure_next_rows(wl, peak_kind_gbs, iters=50):
     out = {}
     stream = torch.cuda.current_stream()
     for name, rows, nbytes, fn in cases:
-        for _ in range(3):
+        for _ in range(3 if evict else 0):
             fn()
             wl.nvfp4() if rows == FP8_ROWS else wl.fp8()  # evict this call's inputs from L2
         evs = []
@@ -424,7 +431,8 @@ def measure_next_rows(wl, peak_kind_gbs, iters=50):
             fn()
             b.record(stream)
             evs.append((a, b))
-            wl.nvfp4() if rows == FP8_ROWS else wl.fp8()
+            if evict:
+                wl.nvfp4() if rows == FP8_ROWS else wl.fp8()
         torch.cuda.synchronize()
         ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
         gbs = nbytes / (ms / 1e3) / 1e9
@@ -629,7 +637,7 @@ _QK_SOURCES = ["include/rq.h", "nvfp4_quant_gb300/csrc/rq_launch.h",
                "nvfp4_quant_gb300/csrc/rq_device.cuh", "nvfp4_quant_gb300/csrc/rq_qk.cu"]
 KERNEL_SOURCES = {"add_rmsnorm_nvfp4": _ROW_SOURCES, "add_rmsnorm_fp8": _ROW_SOURCES,
                   "add_rmsnorm_nvfp4_swizzled": _ROW_SOURCES, "gated_rmsnorm_nvfp4": _ROW_SOURCES,
-                  "qk_rmsnorm_rope_fp8": _QK_SOURCES}
+                  "qk_rmsnorm_rope_fp8": _QK_SOURCES, "qk_rmsnorm_rope_fp8_kv_store_mixed": _QK_SOURCES}
 
 
 def source_hash(kernel):
@@ -804,6 +812,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="for profiler captures: the timed step, then one launch of each call "
+                         "beyond the step; no end-to-end leg, small configurations or CPU baseline")
     args = ap.parse_args()
     if args.warmup < 3:
         print("bench: at least 3 warm-up steps are required", file=sys.stderr)
