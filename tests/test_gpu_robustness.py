@@ -114,8 +114,9 @@ def test_concurrent_calls_from_two_threads():
 
 def test_every_call_captures_into_one_graph():
     """Every entry point (static, dynamic, per-token, swizzled, gated, Q/K,
-    KV pool) captured in one CUDA graph; a replay reproduces the eager
-    outputs bit for bit (the kernels are deterministic)."""
+    Q/K amax and dynamic, uniform and mixed KV pools) captured in one CUDA
+    graph; a replay reproduces the eager outputs bit for bit (the kernels
+    are deterministic)."""
     rows, H = 300, 2048
     x, r, w = synth.rows_input(50, rows, H, "bf16")
     xd, rd, wd = dev16(x, "bf16"), dev16(r, "bf16"), dev16(w, "bf16")
@@ -130,7 +131,10 @@ def test_every_call_captures_into_one_graph():
            "sfz": u8(rq.rq_nvfp4_swizzled_scale_bytes(rows, H)), "rs": f32(rows), "s1": f32(1),
            "s2": f32(1), "am": f32(1), "gp": u8(rows, H // 2), "gsf": u8(rows, H // 16),
            "qo": u8(T, Hq, D), "pool": u8(2 * T, Hk, D), "gzp": u8(rows, H // 2),
-           "gzs": u8(rq.rq_nvfp4_swizzled_scale_bytes(rows, H))}
+           "gzs": u8(rq.rq_nvfp4_swizzled_scale_bytes(rows, H)), "qo2": u8(T, Hq, D),
+           "ko2": u8(T, Hk, D), "qa": f32(1), "ka": f32(1), "qs": f32(1), "ks": f32(1),
+           "qo3": u8(T, Hq, D), "mpool": u8(2 * T, Hk, D + 64)}
+    cs64 = torch.from_numpy(synth.rope_cos_sin(T, 64, 1.0e6)).cuda()
     gs, sc = f32dev(300.0), f32dev(0.02)
     slots = torch.randperm(2 * T, generator=torch.Generator().manual_seed(1))[:T].cuda()
 
@@ -146,6 +150,11 @@ def test_every_call_captures_into_one_graph():
         rq.rq_gated_rmsnorm_nvfp4_swizzled(xd, rd, wd, 1e-6, gs, out["gzp"], out["gzs"])
         rq.rq_qk_rmsnorm_rope_fp8_kv_store(qd, kd, qwd, kwd, 1e-6, posd, csd, sc, sc, out["qo"],
                                            out["pool"], slots)
+        rq.rq_qk_rmsnorm_rope_amax(qd, kd, qwd, kwd, 1e-6, posd, csd, out["qa"], out["ka"])
+        rq.rq_qk_rmsnorm_rope_fp8_dynamic(qd, kd, qwd, kwd, 1e-6, posd, csd, out["qs"], out["ks"],
+                                          out["qo2"], out["ko2"])
+        rq.rq_qk_rmsnorm_rope_fp8_kv_store_mixed(qd, kd, qwd, kwd, 1e-6, posd, cs64, sc, sc,
+                                                 out["qo3"], out["mpool"], slots, 64)
 
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
