@@ -574,6 +574,88 @@ __device__ __forceinline__ uint4 silu_gate8(const uint4 &zv, bool valid = true)
     return pack8<DT>(v);
 }
 
+// ---------------------------------------------------------------- bf16 gate table
+// For bf16 the gated kernel takes its gates from a table in shared memory:
+// the exact gates (silu_gate8) of every bf16 value with |z| in [2^-23, 2^9)
+// (exponent fields 104 .. 135), both signs, 2 * 4096 entries (16 KB), built
+// by each CTA at start (about 1 % of the work of the 16,384 x 7168 call).  A
+// vector's gates are then 8 shared-memory loads instead of 8 fast SiLUs and
+// their near-tie tests.  The values outside the table have closed forms
+// (gate8_bf16).
+constexpr uint32_t kGateLo = 104u << 7;  // bf16 pattern of 2^-23
+constexpr int kGateHalf = 4096;          // entries per sign
+
+__device__ __forceinline__ void gate_table_fill(uint16_t *tab)
+{
+    for (int v = threadIdx.x; v < 2 * kGateHalf / 8; v += blockDim.x) {
+        const uint32_t e0 = 8u * v;
+        const uint32_t b0 = (e0 & (kGateHalf - 1)) + kGateLo + ((e0 & kGateHalf) ? 0x8000u : 0u);
+        const uint4 zv = make_uint4(b0 | ((b0 + 1) << 16), (b0 + 2) | ((b0 + 3) << 16),
+                                    (b0 + 4) | ((b0 + 5) << 16), (b0 + 6) | ((b0 + 7) << 16));
+        sts16(tab + e0, silu_gate8<BF16>(zv));
+    }
+}
+
+// The exact gates dt(RN32(silu(z))) of 8 bf16 values, from the table where
+// all 8 lie in it.  Per 32-bit word (two values), (w & 0x7FFF7FFF) - kGateLo
+// in each half is the table index, in range when bits 12..15 of each half are
+// clear (a half below the range borrows and sets them; the vector then takes
+// the closed forms); the sign bit, moved to bit 12 of its half, selects the
+// second half of the table.  Outside the table:
+//   |z| < 2^-23:  silu(z) = z/2 + z^2/4 + O(z^4), the second term below
+//                 2^-24 |z/2|.  Where z/2 is a bf16 value, every number that
+//                 close to it rounds to it; where z/2 is a bf16 midpoint (z
+//                 in the lowest binades), z^2/4 is far below fp32's smallest
+//                 step, so RN32(silu(z)) is z/2 itself and the dtype rounds
+//                 that tie to even.  Either way the gate is dt(z/2), with z/2
+//                 exact in fp32 (signed zeros included);
+//   |z| >= 512:   e^-|z| < 2^-738: RN32(silu(z)) is z for z > 0 and -0 for
+//                 z < 0;
+//   inf, NaN:     not defined inputs (+inf gives inf, -inf -0, NaN NaN).
+// tests/cuda/silu_check.cu checks this function against the oracle's gate
+// for every bf16 value.
+__device__ __forceinline__ uint4 gate8_bf16(const uint4 &zv, const uint16_t *tab)
+{
+    const uint32_t w[4] = {zv.x, zv.y, zv.z, zv.w};
+    uint32_t t[4], bad = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t m = (w[k] & 0x7FFF7FFFu) - kGateLo * 0x10001u;
+        bad |= m;
+        t[k] = m + ((w[k] >> 3) & 0x10001000u);
+    }
+    uint32_t r[4];
+    if ((bad & 0xF000F000u) == 0) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            uint16_t a, b;
+            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(a) : "r"(smem_addr(tab + (t[k] & 0xFFFFu))));
+            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(b) : "r"(smem_addr(tab + (t[k] >> 16))));
+            r[k] = (uint32_t)a | ((uint32_t)b << 16);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float g[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t b = (w[k] >> (16 * h)) & 0xFFFFu;
+                const float z = __uint_as_float(b << 16);
+                const uint32_t i = (b & 0x7FFFu) - kGateLo;
+                if (i < (uint32_t)kGateHalf) {
+                    g[h] = __uint_as_float((uint32_t)tab[i + ((b >> 15) ? kGateHalf : 0)] << 16);
+                } else if ((b & 0x7FFFu) < kGateLo) {
+                    g[h] = __fmul_rn(z, 0.5f);
+                } else {
+                    g[h] = z > 0.0f ? z : (z < 0.0f ? -0.0f : z);  // NaN stays NaN
+                }
+            }
+            r[k] = BF16::pack(g[0], g[1]);
+        }
+    }
+    return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
 // Elementwise product of two vectors of 8 dtype values, each rounded to
 // nearest even in the dtype.  The fp32 product of two bf16 (fp16) values is
 // exact, so this is the fp32 product rounded to the dtype.

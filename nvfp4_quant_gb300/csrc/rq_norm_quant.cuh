@@ -26,6 +26,8 @@
 #include "rq_device.cuh"
 #include "rq_launch.h"
 
+#include <type_traits>
+
 namespace rq {
 
 template <int G>
@@ -129,6 +131,13 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
     const Divisor by_scale(scale);  // FP8: y / scale
     const Divisor by_six(6.0f);     // NVFP4: (gs * amax) / 6
     const bool sf_words = (p.hidden % 64) == 0;  // 4 block scales per 32-bit store
+    // gated bf16: the gate table in shared memory
+    constexpr bool kGateTab = is_gated<MODE>() && std::is_same<DT, BF16>::value;
+    __shared__ __align__(16) uint16_t gtab[kGateTab ? 2 * kGateHalf : 8];
+    if (kGateTab) {
+        gate_table_fill(gtab);
+        __syncthreads();
+    }
     float amax_acc = 0.0f;
     int parity = 0;
 
@@ -161,7 +170,10 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
             float a[8];
             if (is_gated<MODE>()) {
                 const bool ok = row_ok && j * G + t < nvec;
-                sv[j] = mul8<DT>(xv[j], silu_gate8<DT>(sv[j], ok));  // the gate rounded to dt
+                // the gate rounded to the dtype: from the table (bf16) or the
+                // fast SiLU with its exact path (fp16)
+                const uint4 gate = kGateTab ? gate8_bf16(sv[j], gtab) : silu_gate8<DT>(sv[j], ok);
+                sv[j] = mul8<DT>(xv[j], gate);
             } else {
                 float b[8];
                 unpack8<DT>(xv[j], a);
