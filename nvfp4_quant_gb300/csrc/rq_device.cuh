@@ -321,9 +321,11 @@ __device__ __forceinline__ float div_by(float a, const Divisor &d)
     return copysignf(fma_rn(r, d.y, q), a);
 }
 
-// |a| / b for two dividends with Blackwell's packed fp32 ops, rounded as the
-// IEEE quotient (the steps of div_by without the final copysign; callers put
-// the sign back on the encoded result).
+// |a| / b for two dividends with Blackwell's packed fp32 ops: the steps of
+// div_by on |a| without the final copysign (callers put the sign back on the
+// encoded result).  Each step is the same IEEE operation on both halves
+// (fma(q, -b, m) equals fma(-q, b, m) exactly, negation being exact), so
+// every magnitude is bit for bit div_by's.
 template <bool kFast>
 __device__ __forceinline__ float2 div_mag_by2(float2 a, const Divisor &d)
 {
@@ -335,24 +337,6 @@ __device__ __forceinline__ float2 div_mag_by2(float2 a, const Divisor &d)
     const float2 q = __fmul2_rn(m, y2);
     const float2 r = __ffma2_rn(q, make_float2(-d.b, -d.b), m);
     return __ffma2_rn(r, y2, q);
-}
-
-// The same division for two dividends with Blackwell's packed fp32 ops: each
-// step is the same IEEE operation on both halves (fma(q, -b, m) equals
-// fma(-q, b, m) exactly, negation being exact), so every result is bit for
-// bit div_by's.
-template <bool kFast>
-__device__ __forceinline__ float2 div_by2(float2 a, const Divisor &d)
-{
-    if (!kFast) return make_float2(div_rn(a.x, d.b), div_rn(a.y, d.b));
-    float2 m;
-    asm("{ .reg .f32 t; abs.f32 t, %1; min.NaN.f32 %0, t, %2; }" : "=f"(m.x) : "f"(a.x), "f"(d.clamp));
-    asm("{ .reg .f32 t; abs.f32 t, %1; min.NaN.f32 %0, t, %2; }" : "=f"(m.y) : "f"(a.y), "f"(d.clamp));
-    const float2 y2 = make_float2(d.y, d.y);
-    const float2 q = __fmul2_rn(m, y2);
-    const float2 r = __ffma2_rn(q, make_float2(-d.b, -d.b), m);
-    const float2 t = __ffma2_rn(r, y2, q);
-    return make_float2(copysignf(t.x, a.x), copysignf(t.y, a.y));
 }
 
 // ---------------------------------------------------------------- SiLU gate

@@ -3,9 +3,11 @@
 // every finite fp32 dividend, for each divisor given on the command line.
 // Prints, per divisor: the fp32 quotients that differ where the reference
 // quotient has magnitude in [2^-40, 2^20), the E4M3 codes (satfinite)
-// that differ anywhere, NaN and infinite dividends included, and the results
-// of the packed two-wide version (rq::div_by2, on the pair (a, -a)) that are
-// not bit for bit the scalar version's.  Built and run by tests/test_gpu_division.py.
+// that differ anywhere, NaN and infinite dividends included, and, for the
+// packed two-wide magnitude version the Q/K kernel uses (rq::div_mag_by2 on
+// the pair (a, -a), with the sign of a put back on the E4M3 code byte), the
+// non-NaN dividends whose magnitudes are not bit for bit |div_by(a)| or whose
+// codes are not the scalar version's.  Built and run by tests/test_gpu_division.py.
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -32,11 +34,15 @@ __global__ void check(float b)
         if ((rq::e4m3x2(ref, 0.0f) & 0xFF) != (rq::e4m3x2(got, 0.0f) & 0xFF))
             atomicAdd(&g_code_diff, 1ull);
         const float na = __uint_as_float(bits ^ 0x80000000u);
-        const float got_n = d.fast ? rq::div_by<true>(na, d) : rq::div_by<false>(na, d);
-        const float2 g2 = d.fast ? rq::div_by2<true>(make_float2(a, na), d)
-                                 : rq::div_by2<false>(make_float2(a, na), d);
-        if (__float_as_uint(g2.x) != __float_as_uint(got) || __float_as_uint(g2.y) != __float_as_uint(got_n))
-            atomicAdd(&g_pack_diff, 1ull);
+        const float2 g2 = d.fast ? rq::div_mag_by2<true>(make_float2(a, na), d)
+                                 : rq::div_mag_by2<false>(make_float2(a, na), d);
+        if (!isnan(a)) {
+            const unsigned int mag = __float_as_uint(got) & 0x7FFFFFFFu;
+            const unsigned int code = (rq::e4m3x2(g2.x, 0.0f) & 0xFFu) | ((bits >> 24) & 0x80u);
+            if (__float_as_uint(g2.x) != mag || __float_as_uint(g2.y) != mag ||
+                code != (rq::e4m3x2(got, 0.0f) & 0xFFu))
+                atomicAdd(&g_pack_diff, 1ull);
+        }
     }
 }
 

@@ -3,7 +3,9 @@ reciprocal and one FMA correction (Markstein's theorem) instead of a full
 division per element.  This test compares that division with CUDA's correctly
 rounded __fdiv_rn over every fp32 dividend: the quotients must agree bit for
 bit wherever the quotient's magnitude is in [2^-40, 2^20), and the E4M3 codes
-everywhere (NaN and infinite dividends included)."""
+everywhere (NaN and infinite dividends included).  The packed two-wide
+magnitude version that the Q/K kernel uses, with the sign put back on the
+code byte, must give the scalar version's magnitudes and codes."""
 import os
 import subprocess
 
@@ -37,4 +39,4 @@ def test_shared_divisor_division_is_correctly_rounded(tmp_path):
     for f in lines:
         assert f[3] == "0", "quotient differs from __fdiv_rn: " + " ".join(f)
         assert f[5] == "0", "E4M3 code differs: " + " ".join(f)
-        assert f[9] == "0", "packed two-wide division differs from the scalar one: " + " ".join(f)
+        assert f[9] == "0", "packed magnitude division differs from the scalar one: " + " ".join(f)
