@@ -11,7 +11,12 @@
  *  - Scales are fp32 scalars in device memory, read by the kernel, so a call
  *    never synchronises with the host.
  *  - Work is enqueued on `stream` (NULL = the legacy default stream) and is
- *    asynchronous: a returned RQ_OK means the launch was accepted.
+ *    asynchronous: a returned RQ_OK means the launch was accepted.  Kernels
+ *    are launched with programmatic stream serialisation: their thread
+ *    blocks may be scheduled while the previous kernel in the stream is
+ *    finishing, and wait for it to complete before their first memory
+ *    access, so stream order holds as for a plain launch (also under graph
+ *    capture, where the dependency is a programmatic edge).
  *  - Every argument check runs on the host before any CUDA call; a failed
  *    check returns an error status and launches nothing.  Nothing throws
  *    across the ABI.  A call with rows == 0 (or n_tokens == 0) returns RQ_OK

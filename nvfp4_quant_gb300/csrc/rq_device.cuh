@@ -8,6 +8,22 @@
 
 namespace rq {
 
+// ---------------------------------------------------- dependent launches
+// Every kernel of the library is launched with programmatic stream
+// serialisation allowed, so that its CTAs can be scheduled while the previous
+// kernel in the stream drains.  pdl_wait() returns once that kernel has
+// finished and its writes are visible; each kernel calls it before its first
+// global memory access of any kind.  pdl_trigger() lets the next kernel be
+// scheduled as soon as every CTA of this one has called it (it changes when
+// the next kernel starts, never what it sees: that kernel waits in turn).
+// Both are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_trigger()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- memory
 // Streaming 16-byte load of data read exactly once (x, residual): no L1
 // allocation.  Plain (coherent) load, so it is also correct for the residual

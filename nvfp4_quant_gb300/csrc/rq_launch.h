@@ -98,6 +98,27 @@ __host__ __device__ constexpr bool is_swizzled()
 // SM count of device `dev` (cached).
 int device_sms(int dev);
 
+// Launch with programmatic stream serialisation allowed: the kernel's CTAs may
+// be scheduled before the previous kernel in the stream has finished (each
+// kernel waits for it with pdl_wait() before touching global memory).  Under
+// stream capture this records a programmatic edge in the graph.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                       cudaStream_t stream, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 template <typename DT, int MODE>
 cudaError_t launch_add_rmsnorm(const NormQuantParams &p, cudaStream_t stream);
 

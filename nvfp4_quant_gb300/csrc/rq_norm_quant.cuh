@@ -119,6 +119,16 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
     const int nvec = p.nvec;
     const int64_t H = p.hidden;
 
+    // gated bf16: the gate table in shared memory, computed (no global memory
+    // access) while the previous kernel in the stream may still be running
+    constexpr bool kGateTab = is_gated<MODE>() && std::is_same<DT, BF16>::value;
+    __shared__ __align__(16) uint16_t gtab[kGateTab ? 2 * kGateHalf : 8];
+    if (kGateTab) {
+        gate_table_fill(gtab);
+        __syncthreads();
+    }
+    pdl_wait();
+
     // weight vectors of this thread, kept for every row it processes
     uint4 wv[VPT];
 #pragma unroll
@@ -131,13 +141,6 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
     const Divisor by_scale(scale);  // FP8: y / scale
     const Divisor by_six(6.0f);     // NVFP4: (gs * amax) / 6
     const bool sf_words = (p.hidden % 64) == 0;  // 4 block scales per 32-bit store
-    // gated bf16: the gate table in shared memory
-    constexpr bool kGateTab = is_gated<MODE>() && std::is_same<DT, BF16>::value;
-    __shared__ __align__(16) uint16_t gtab[kGateTab ? 2 * kGateHalf : 8];
-    if (kGateTab) {
-        gate_table_fill(gtab);
-        __syncthreads();
-    }
     float amax_acc = 0.0f;
     int parity = 0;
 
@@ -325,6 +328,8 @@ __global__ void __launch_bounds__(GroupShape<G>::kBlock, (min_ctas_per_sm<G, VPT
 add_rmsnorm_quant_kernel(const NormQuantParams p)
 {
     __shared__ float red[2][GroupShape<G>::kWarps];
+    pdl_trigger();
+    if (MODE == MODE_FP8) pdl_wait();  // before the scale load; the body waits in any case
     if (MODE == MODE_FP8 && !Divisor(ld_f32(p.scale)).fast)
         add_rmsnorm_quant_body<DT, G, VPT, MODE, false>(p, red);
     else

@@ -38,8 +38,7 @@ static cudaError_t launch_cfg(const NormQuantParams &p, cudaStream_t stream)
     const int64_t groups = (p.rows + S::kRowsPerCta - 1) / S::kRowsPerCta;
     const int64_t full = (int64_t)device_sms(dev) * per_sm;
     const int grid = (int)(groups < full ? groups : full);
-    kern<<<grid, S::kBlock, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, S::kBlock, 0, stream, p);
 }
 
 // Long rows through shared memory: 4 * hidden bytes of dynamic shared memory
@@ -73,8 +72,7 @@ static cudaError_t launch_staged(const NormQuantParams &p, cudaStream_t stream)
     }
     const int64_t full = (int64_t)device_sms(dev) * per_sm;
     const int grid = (int)(p.rows < full ? p.rows : full);
-    kern<<<grid, kStagedThreads, smem, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, kStagedThreads, smem, stream, p);
 }
 
 // Thread-group shape by row length (nvec 16-byte vectors per row): with at

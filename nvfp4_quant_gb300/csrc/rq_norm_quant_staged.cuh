@@ -201,6 +201,8 @@ add_rmsnorm_quant_staged_kernel(const NormQuantParams p)
 {
     __shared__ float red[2][kStagedThreads / 32];
     extern __shared__ uint4 buf[];  // 2 * nvec vectors: x then residual
+    pdl_trigger();
+    pdl_wait();
     if (MODE == MODE_FP8 && !Divisor(ld_f32(p.scale)).fast)
         staged_body<DT, MODE, false>(p, buf, red);
     else

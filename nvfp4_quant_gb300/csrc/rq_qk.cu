@@ -247,6 +247,8 @@ __global__ void __launch_bounds__(kQKBlock, 6)
 qk_rmsnorm_rope_kernel(const QKParams p)
 {
     __shared__ float red[kQKBlock / 32][2];
+    pdl_trigger();
+    pdl_wait();
     const bool fast = QMODE == QK_AMAX || ((p.hq == 0 || Divisor(ld_f32(p.q_scale)).fast) &&
                                           (p.hk == 0 || Divisor(ld_f32(p.k_scale)).fast));
     if (fast)
@@ -274,8 +276,7 @@ cudaError_t launch_qk_rmsnorm_rope(const QKParams &p, cudaStream_t stream)
     const int64_t need = (p.n_tokens * groups * 32 + kQKBlock - 1) / kQKBlock;  // a warp per unit
     const int64_t full = (int64_t)device_sms(dev) * per_sm;
     const int grid = (int)(need < full ? need : full);
-    kern<<<grid, kQKBlock, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, kQKBlock, 0, stream, p);
 }
 
 #define RQ_QK_INSTANTIATE(DT)                                                                      \
@@ -288,6 +289,8 @@ RQ_QK_INSTANTIATE(FP16)
 // ---- scales from a calibrated amax: one fp32 IEEE division each
 __global__ void scale_from_amax_kernel(const float *amax, float *out, int nvfp4, int zero_to_one)
 {
+    pdl_trigger();
+    pdl_wait();
     const float a = *amax;  // plain load: out may alias amax
     *out = (zero_to_one && !(a > 0.0f)) ? 1.0f : nvfp4 ? __fdiv_rn(2688.0f, a) : __fdiv_rn(a, 448.0f);
 }
@@ -295,8 +298,7 @@ __global__ void scale_from_amax_kernel(const float *amax, float *out, int nvfp4,
 cudaError_t launch_scale_from_amax(const float *amax, float *out, int nvfp4, int zero_to_one,
                                    cudaStream_t stream)
 {
-    scale_from_amax_kernel<<<1, 1, 0, stream>>>(amax, out, nvfp4, zero_to_one);
-    return cudaGetLastError();
+    return launch_pdl(scale_from_amax_kernel, 1, 1, 0, stream, amax, out, nvfp4, zero_to_one);
 }
 
 }  // namespace rq
