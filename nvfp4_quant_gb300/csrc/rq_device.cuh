@@ -628,10 +628,9 @@ __device__ __forceinline__ uint4 gate8_bf16(const uint4 &zv, const uint16_t *tab
     if ((bad & 0xF000F000u) == 0) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            uint16_t a, b;
-            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(a) : "r"(smem_addr(tab + (t[k] & 0xFFFFu))));
-            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(b) : "r"(smem_addr(tab + (t[k] >> 16))));
-            r[k] = (uint32_t)a | ((uint32_t)b << 16);
+            // plain loads: the table is not written after it is filled, so
+            // the compiler may schedule them freely
+            r[k] = (uint32_t)tab[t[k] & 0xFFFFu] | ((uint32_t)tab[t[k] >> 16] << 16);
         }
     } else {
 #pragma unroll

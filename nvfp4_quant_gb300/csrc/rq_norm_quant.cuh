@@ -141,6 +141,16 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
     const Divisor by_scale(scale);  // FP8: y / scale
     const Divisor by_six(6.0f);     // NVFP4: (gs * amax) / 6
     const bool sf_words = (p.hidden % 64) == 0;  // 4 block scales per 32-bit store
+    // NVFP4: enc = scale / sf for each of the 256 E4M3 scale bytes (0 where
+    // sf is 0), one correctly rounded division each, looked up per block
+    __shared__ float enc_tab[is_nvfp4<MODE>() ? 256 : 1];
+    if (is_nvfp4<MODE>()) {
+        for (int c = tid; c < 256; c += S::kBlock) {
+            const float sfv = e4m3_value(c);
+            enc_tab[c] = sfv == 0.0f ? 0.0f : __fdiv_rn(scale, sfv);
+        }
+        __syncthreads();
+    }
     float amax_acc = 0.0f;
     int parity = 0;
 
@@ -166,8 +176,9 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
         }
 
         // ---- residual' = dt(x + r), stored (gated: g = dt(x * dt(silu(z))),
-        // not stored); sum of squares of the rounded values
-        float ss = 0.0f;
+        // not stored); sum of squares of the rounded values, as two partial
+        // sums (even and odd elements) in one packed fp32 FMA per pair
+        float2 sq = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
             float a[8];
@@ -187,13 +198,17 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
             }
             unpack8<DT>(sv[j], a);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ss = __fmaf_rn(a[e], a[e], ss);  // squares are exact
+            for (int i = 0; i < 4; ++i) {
+                const float2 ai = make_float2(a[2 * i], a[2 * i + 1]);
+                sq = __ffma2_rn(ai, ai, sq);  // squares are exact
+            }
             const int k = j * G + t;
             if (MODE != MODE_AMAX && !is_gated<MODE>() && row_ok && k < nvec)
                 st16(static_cast<uint8_t *>(p.res_out) + (row * H + (int64_t)k * 8) * 2, sv[j]);
         }
 
         // ---- row reduction
+        float ss = __fadd_rn(sq.x, sq.y);
         if (G <= 32) {
             ss = group_sum<(G <= 32 ? G : 32)>(ss);
         } else {
@@ -211,6 +226,7 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
 
         // ---- normalise, store, quantise
         float row_amax = 0.0f;  // per-token mode: max |y| of this thread's part of the row
+        const float2 r2 = make_float2(rstd, rstd);
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
             const int k = j * G + t;
@@ -218,8 +234,22 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
             float s[8], w[8], y[8];
             unpack8<DT>(sv[j], s);
             unpack8<DT>(wv[j], w);
+            // (s * rstd) * w, each product rounded: packed pairs, except in the
+            // swizzled NVFP4 mode, where the scalar form measured faster on GB300
+            // (166 against 176 us on 16,384 x 7168; as with the swizzled row
+            // offset above, the packed form delays the next row's loads)
+            if (MODE == MODE_NVFP4_SWZ) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) y[e] = __fmul_rn(__fmul_rn(s[e], rstd), w[e]);
+                for (int e = 0; e < 8; ++e) y[e] = __fmul_rn(__fmul_rn(s[e], rstd), w[e]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 yi = __fmul2_rn(__fmul2_rn(make_float2(s[2 * i], s[2 * i + 1]), r2),
+                                                 make_float2(w[2 * i], w[2 * i + 1]));
+                    y[2 * i] = yi.x;
+                    y[2 * i + 1] = yi.y;
+                }
+            }
             const uint4 yv = pack8<DT>(y);
             if (MODE != MODE_AMAX && p.norm_out != nullptr && ok)
                 st16(static_cast<uint8_t *>(p.norm_out) + (row * H + (int64_t)k * 8) * 2, yv);
@@ -238,11 +268,15 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
                 const float a = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));  // 16-element block
                 const float t2 = div_by<true>(__fmul_rn(scale, a), by_six);
                 const uint32_t sfc = e4m3x2(t2, 0.0f) & 0xFFu;
-                const float sfv = e4m3_value(sfc);
-                const float enc = sfv == 0.0f ? 0.0f : __fdiv_rn(scale, sfv);
+                const float enc = enc_tab[sfc];
+                const float2 enc2 = make_float2(enc, enc);
                 float v[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(y[e], enc);
+                for (int i = 0; i < 4; ++i) {
+                    const float2 vi = __fmul2_rn(make_float2(y[2 * i], y[2 * i + 1]), enc2);
+                    v[2 * i] = vi.x;
+                    v[2 * i + 1] = vi.y;
+                }
                 const uint32_t codes = e2m1x8(v);
                 if (ok) st4(p.q + row * (H / 2) + (int64_t)k * 4, codes);
                 store_block_scale<is_swizzled<MODE>()>(p, row, k, ok, sfc, sf_words);
@@ -313,7 +347,8 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
     }
 }
 
-// Register budget: the 128-thread shapes with 7 or 8 vectors per thread hold
+// Register budget: the gated call's 448 x 2 shape is held to two CTAs per SM
+// (70 registers).  The 128-thread shapes with 7 or 8 vectors per thread hold
 // about 167 registers; past 170 only two CTAs fit per SM and the NVFP4 call on
 // 16,384 x 7168 slows from 160 to 195 us, so they are held to three CTAs.
 // Every other shape passes 0 (no minimum), which leaves ptxas its own
@@ -321,7 +356,10 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
 // registers, and the 32 x 4 shape went from 96 to 152 registers (five CTAs per
 // SM down to three) and 32,768 x 2048 from 95 to 107 us.
 template <int G, int VPT>
-constexpr int min_ctas_per_sm() { return (G == 128 && VPT >= 7) ? 3 : 0; }
+constexpr int min_ctas_per_sm()
+{
+    return (G == 128 && VPT >= 7) ? 3 : (G == 448 && VPT == 2) ? 2 : 0;
+}
 
 template <typename DT, int G, int VPT, int MODE>
 __global__ void __launch_bounds__(GroupShape<G>::kBlock, (min_ctas_per_sm<G, VPT>()))

@@ -174,3 +174,81 @@ def test_every_call_captures_into_one_graph():
     torch.cuda.synchronize()
     for key in out:
         assert torch.equal(out[key], eager[key]), key
+
+
+def test_back_to_back_calls_see_each_others_writes():
+    """Each kernel may be scheduled while the previous one in the stream
+    drains, and waits for it before touching memory.  A chain of in-place
+    calls where every call reads the buffer the previous call wrote and
+    overwrites the one it read, with no synchronisation between them (eager
+    and replayed from a graph), gives the oracle's chain bit for bit; so does
+    a Q/K call on codes' inputs that a row call wrote just before it."""
+    rows, H, n = 4096, 2048, 6
+    a, b, w = synth.rows_input(60, rows, H, "bf16")
+    # oracle chain: even calls b <- a + b, odd calls a <- b + a
+    ha, hb = a.copy(), b.copy()
+    q_ref = []
+    for i in range(n):
+        x, r = (ha, hb) if i % 2 == 0 else (hb, ha)
+        s_ref, _, qr = O.add_rmsnorm_fp8("bf16", x, r, w, 1e-6, 0.05)
+        q_ref.append(qr)
+        if i % 2 == 0:
+            hb = s_ref
+        else:
+            ha = s_ref
+    wd, sc = dev16(w, "bf16"), f32dev(0.05)
+    A, B = dev16(a, "bf16"), dev16(b, "bf16")
+    qs = [torch.empty((rows, H), dtype=torch.uint8, device="cuda") for _ in range(n)]
+
+    def chain():
+        for i in range(n):
+            x, r = (A, B) if i % 2 == 0 else (B, A)
+            rq.rq_add_rmsnorm_fp8(x, r, r, wd, 1e-6, sc, qs[i])
+
+    def check(tag):
+        torch.cuda.synchronize()
+        assert np.array_equal(host16(A), ha), tag
+        assert np.array_equal(host16(B), hb), tag
+        for i in range(n):
+            assert_codes(host8(qs[i]), q_ref[i], 0x80, "%s: codes of call %d" % (tag, i))
+
+    chain()
+    check("eager")
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        g.capture_begin()
+        chain()
+        g.capture_end()
+    torch.cuda.current_stream().wait_stream(s)
+    A.copy_(dev16(a, "bf16"))
+    B.copy_(dev16(b, "bf16"))
+    for t in qs:
+        t.zero_()
+    g.replay()
+    check("graph")
+
+    # a row call writes the Q/K call's Q input in place, the Q/K call reads it
+    # right after
+    T, Hq, Hk, D = 512, 8, 4, 128
+    q, k, qw, kw, pos, cs = synth.qk_input(61, T, Hq, Hk, D, "bf16")
+    q2 = q.reshape(T, Hq * D)
+    zero = np.zeros_like(q2)
+    ones = np.ones(Hq * D, np.float32).view(np.uint32) >> 16  # bf16 1.0
+    q_in, _, _ = O.add_rmsnorm_fp8("bf16", q2, zero, ones.astype(np.uint16), 1e-6, 0.05)
+    zd = dev16(zero, "bf16")
+    q8 = torch.empty((T, Hq * D), dtype=torch.uint8, device="cuda")
+    qo, ko = (torch.empty((T, h, D), dtype=torch.uint8, device="cuda") for h in (Hq, Hk))
+    rq.rq_add_rmsnorm_fp8(dev16(q2, "bf16"), zd, zd, dev16(ones.astype(np.uint16), "bf16"), 1e-6,
+                          sc, q8)
+    rq.rq_qk_rmsnorm_rope_fp8(zd.view(T, Hq, D), dev16(k, "bf16"), dev16(qw, "bf16"),
+                              dev16(kw, "bf16"), 1e-6, torch.from_numpy(pos).cuda(),
+                              torch.from_numpy(cs).cuda(), sc, sc, qo, ko)
+    torch.cuda.synchronize()
+    _, qq_ref = O.qk_rmsnorm_rope_fp8("bf16", q_in.reshape(-1), Hq * D, T, Hq, D, qw, 1e-6, pos,
+                                      cs, 0.05)
+    _, kq_ref = O.qk_rmsnorm_rope_fp8("bf16", k.reshape(-1), Hk * D, T, Hk, D, kw, 1e-6, pos, cs,
+                                      0.05)
+    assert_codes(host8(qo).reshape(qq_ref.shape), qq_ref, 0x80, "Q codes after a row call")
+    assert_codes(host8(ko).reshape(kq_ref.shape), kq_ref, 0x80, "K codes after a row call")
