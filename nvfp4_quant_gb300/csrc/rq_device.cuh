@@ -655,6 +655,71 @@ __device__ __forceinline__ uint4 gate8_bf16(const uint4 &zv, const uint16_t *tab
     return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
+// ---------------------------------------------------------------- fp16 gate table
+// The same for fp16, where the table must reach further: it holds the exact
+// gates of every fp16 value with |z| < 32 (exponent fields 0 .. 19,
+// subnormals included), both signs, 2 * 20,480 entries (80 KB, in dynamic
+// shared memory).  Outside it:
+//   z >= 32:   e^-z < 2^-46, so z * sigma(z) is within 2^-46 |z| of z and
+//              RN32(silu(z)) = z;
+//   z <= -32:  |silu(z)| < 32 e^-32 < 2^-41, far below half the smallest fp16
+//              subnormal (2^-25): the gate is -0;
+//   inf, NaN:  as for bf16.
+// tests/cuda/silu_check.cu checks gate8_fp16 against the oracle's gate for
+// every fp16 value.
+constexpr int kGateHalfF16 = 20 << 10;  // entries per sign
+
+__device__ __forceinline__ void gate_table_fill_fp16(uint16_t *tab)
+{
+    for (int v = threadIdx.x; v < 2 * kGateHalfF16 / 8; v += blockDim.x) {
+        const uint32_t e0 = 8u * v;  // 8 entries, never across the sign boundary
+        const uint32_t b0 = e0 < (uint32_t)kGateHalfF16 ? e0 : (e0 - kGateHalfF16) | 0x8000u;
+        const uint4 zv = make_uint4(b0 | ((b0 + 1) << 16), (b0 + 2) | ((b0 + 3) << 16),
+                                    (b0 + 4) | ((b0 + 5) << 16), (b0 + 6) | ((b0 + 7) << 16));
+        sts16(tab + e0, silu_gate8<FP16>(zv));
+    }
+}
+
+// The exact gates of 8 fp16 values, from the table where all 8 lie in it.
+// Per 32-bit word, the magnitude of each half plus its sign times 20,480 is
+// the table index (at most 40,959, so no carry between the halves); a half
+// with magnitude >= 0x5000 (|z| >= 32) sets bit 15 of magnitude + 0x3000.
+__device__ __forceinline__ uint4 gate8_fp16(const uint4 &zv, const uint16_t *tab)
+{
+    const uint32_t w[4] = {zv.x, zv.y, zv.z, zv.w};
+    uint32_t t[4], bad = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t m = w[k] & 0x7FFF7FFFu;
+        bad |= m + 0x30003000u;
+        t[k] = m + ((w[k] >> 15) & 0x00010001u) * (uint32_t)kGateHalfF16;
+    }
+    uint32_t r[4];
+    if ((bad & 0x80008000u) == 0) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            r[k] = (uint32_t)tab[t[k] & 0xFFFFu] | ((uint32_t)tab[t[k] >> 16] << 16);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float g[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t b = (w[k] >> (16 * h)) & 0xFFFFu;
+                const uint32_t m = b & 0x7FFFu;
+                if (m < 0x5000u) {
+                    g[h] = FP16::lo(tab[m + ((b >> 15) ? kGateHalfF16 : 0)]);
+                } else {
+                    const float z = FP16::lo(b);
+                    g[h] = z > 0.0f ? z : (z < 0.0f ? -0.0f : z);  // NaN stays NaN
+                }
+            }
+            r[k] = FP16::pack(g[0], g[1]);
+        }
+    }
+    return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
 // Elementwise product of two vectors of 8 dtype values, each rounded to
 // nearest even in the dtype.  The fp32 product of two bf16 (fp16) values is
 // exact, so this is the fp32 product rounded to the dtype.

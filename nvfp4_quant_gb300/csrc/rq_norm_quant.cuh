@@ -106,6 +106,20 @@ __device__ __forceinline__ void store_block_scale(const NormQuantParams &p, int6
     }
 }
 
+// Whether a shape takes fp16 gates from a table in dynamic shared memory (the
+// gated call's 448 x 2 shape: two CTAs per SM either way), and its bytes.
+template <typename DT, int G, int MODE>
+__host__ __device__ constexpr bool gate_table_fp16()
+{
+    return is_gated<MODE>() && std::is_same<DT, FP16>::value && G == 448;
+}
+
+template <typename DT, int G, int MODE>
+__host__ __device__ constexpr int dynamic_smem_bytes()
+{
+    return gate_table_fp16<DT, G, MODE>() ? 2 * kGateHalfF16 * 2 : 0;
+}
+
 // kFast: the FP8 divisor is in the range of the branch-free division (the
 // kernel picks the body once; see Divisor).
 template <typename DT, int G, int VPT, int MODE, bool kFast>
@@ -125,6 +139,13 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
     __shared__ __align__(16) uint16_t gtab[kGateTab ? 2 * kGateHalf : 8];
     if (kGateTab) {
         gate_table_fill(gtab);
+        __syncthreads();
+    }
+    // gated fp16 in the 448 x 2 shape: its table in dynamic shared memory
+    constexpr bool kGateTab16 = gate_table_fp16<DT, G, MODE>();
+    extern __shared__ __align__(16) uint16_t gtab16[];
+    if (kGateTab16) {
+        gate_table_fill_fp16(gtab16);
         __syncthreads();
     }
     pdl_wait();
@@ -186,7 +207,9 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
                 const bool ok = row_ok && j * G + t < nvec;
                 // the gate rounded to the dtype: from the table (bf16) or the
                 // fast SiLU with its exact path (fp16)
-                const uint4 gate = kGateTab ? gate8_bf16(sv[j], gtab) : silu_gate8<DT>(sv[j], ok);
+                const uint4 gate = kGateTab     ? gate8_bf16(sv[j], gtab)
+                                   : kGateTab16 ? gate8_fp16(sv[j], gtab16)
+                                                : silu_gate8<DT>(sv[j], ok);
                 sv[j] = mul8<DT>(xv[j], gate);
             } else {
                 float b[8];

@@ -13,13 +13,18 @@ namespace rq {
 constexpr int kMaxDevices = 64;
 
 // Resident CTAs per SM of one kernel instantiation, cached per device.
+// A kernel with more than 48 KB of dynamic shared memory is first allowed it;
+// 0 if that is refused.
 template <typename Kern>
-static int resident_ctas(Kern kern, int block, int dev, std::atomic<int> *cache)
+static int resident_ctas(Kern kern, int block, int dev, std::atomic<int> *cache, int smem = 0)
 {
     int v = dev < kMaxDevices ? cache[dev].load(std::memory_order_relaxed) : 0;
     if (v > 0) return v;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, block, 0) != cudaSuccess || n < 1)
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, block, smem) != cudaSuccess || n < 1)
         n = 1;
     if (dev < kMaxDevices) cache[dev].store(n, std::memory_order_relaxed);
     return n;
@@ -34,11 +39,13 @@ static cudaError_t launch_cfg(const NormQuantParams &p, cudaStream_t stream)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const int per_sm = resident_ctas(kern, S::kBlock, dev, occ_cache);
+    constexpr int smem = dynamic_smem_bytes<DT, G, MODE>();
+    const int per_sm = resident_ctas(kern, S::kBlock, dev, occ_cache, smem);
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;  // the shared memory was refused
     const int64_t groups = (p.rows + S::kRowsPerCta - 1) / S::kRowsPerCta;
     const int64_t full = (int64_t)device_sms(dev) * per_sm;
     const int grid = (int)(groups < full ? groups : full);
-    return launch_pdl(kern, grid, S::kBlock, 0, stream, p);
+    return launch_pdl(kern, grid, S::kBlock, smem, stream, p);
 }
 
 // Long rows through shared memory: 4 * hidden bytes of dynamic shared memory
@@ -101,7 +108,8 @@ cudaError_t launch_add_rmsnorm(const NormQuantParams &p, cudaStream_t stream)
     // The gate's table lookups and SiLU make the gated call's chain per
     // vector long: more, shorter threads per row hide it better (16,384 x 7168
     // bf16: 448 x 2 at 28 warps per SM 155 us, 128 x 7 at 12 warps 168 us,
-    // 512 x 2 at 64 warps 174 us).
+    // 512 x 2 at 64 warps 174 us).  This shape also takes fp16 gates from a
+    // table (80 KB of shared memory per CTA).
     if constexpr (is_gated<MODE>()) {
         if (n > 512 && n <= 896) return launch_cfg<DT, 448, 2, MODE>(p, stream);
     }

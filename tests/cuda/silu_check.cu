@@ -7,11 +7,12 @@
 //     rounded once to fp32.  rq::kSiluUlps, the window of the near-tie test,
 //     must bound it.
 //  2. For bf16 and fp16, the gate dt(silu(z)) that silu_gate8 gives for every
-//     one of the 65,536 bit patterns z, and for bf16 also the gate that the
-//     gated kernel takes from its shared-memory table (gate8_bf16), written to
-//     the file named by argv[1] (65,536 bf16 gates, 65,536 fp16 gates, 65,536
-//     bf16 table gates) for the test to compare with the oracle's, and how
-//     many of the patterns with |z| <= 8 took the exact path.
+//     one of the 65,536 bit patterns z, and the gates that the gated kernels
+//     take from their shared-memory tables (gate8_bf16, gate8_fp16), written
+//     to the file named by argv[1] (65,536 bf16 gates, 65,536 fp16 gates,
+//     65,536 bf16 table gates, 65,536 fp16 table gates) for the test to
+//     compare with the oracle's, and how many of the patterns with |z| <= 8
+//     took the exact path.
 #include <cstdio>
 
 #include "rq_device.cuh"
@@ -85,6 +86,22 @@ __global__ void table_gates(unsigned short *out)
     for (int e = 0; e < 8; ++e) out[b + e] = (unsigned short)(w[e / 2] >> (16 * (e & 1)));
 }
 
+// the same for fp16: its table in dynamic shared memory
+__global__ void table_gates_fp16(unsigned short *out)
+{
+    extern __shared__ __align__(16) uint16_t tab16[];
+    rq::gate_table_fill_fp16(tab16);
+    __syncthreads();
+    const unsigned i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= 65536u / 8) return;
+    const unsigned b = 8 * i;
+    const uint4 zv = make_uint4(b | ((b + 1) << 16), (b + 2) | ((b + 3) << 16),
+                                (b + 4) | ((b + 5) << 16), (b + 6) | ((b + 7) << 16));
+    const uint4 g = rq::gate8_fp16(zv, tab16);
+    const unsigned w[4] = {g.x, g.y, g.z, g.w};
+    for (int e = 0; e < 8; ++e) out[b + e] = (unsigned short)(w[e / 2] >> (16 * (e & 1)));
+}
+
 int main(int argc, char **argv)
 {
     if (argc < 2) {
@@ -94,7 +111,10 @@ int main(int argc, char **argv)
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0);
     unsigned short *d_out = nullptr;
-    if (cudaMalloc(&d_out, 3 * 65536 * sizeof(unsigned short)) != cudaSuccess) {
+    const int tab16_bytes = 2 * rq::kGateHalfF16 * 2;
+    if (cudaFuncSetAttribute(table_gates_fp16, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             tab16_bytes) != cudaSuccess ||
+        cudaMalloc(&d_out, 4 * 65536 * sizeof(unsigned short)) != cudaSuccess) {
         std::printf("error: cudaMalloc\n");
         return 2;
     }
@@ -102,12 +122,13 @@ int main(int argc, char **argv)
     gates<rq::BF16><<<32, 256>>>(d_out, 0);
     gates<rq::FP16><<<32, 256>>>(d_out + 65536, 1);
     table_gates<<<32, 256>>>(d_out + 2 * 65536);
+    table_gates_fp16<<<32, 256, tab16_bytes>>>(d_out + 3 * 65536);
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         std::printf("error %s\n", cudaGetErrorString(e));
         return 2;
     }
-    static unsigned short h[3 * 65536];
+    static unsigned short h[4 * 65536];
     unsigned int mx = 0, slow[2] = {0, 0};
     cudaMemcpy(h, d_out, sizeof(h), cudaMemcpyDeviceToHost);
     cudaMemcpyFromSymbol(&mx, g_max_bits, sizeof(mx));

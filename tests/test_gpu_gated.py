@@ -146,8 +146,8 @@ def test_gate_saturates_and_handles_extreme_gates():
 def test_gate_exact_over_every_dtype_value(tmp_path):
     """The kernel's gate dt(silu(z)) (tests/cuda/silu_check.cu runs the
     library's device code: the fast path with its exact path for both dtypes,
-    and the shared-memory table with its closed forms that the bf16 kernel
-    uses) for every finite bf16 and fp16 value z, bit for bit against the
+    and the shared-memory tables with their closed forms that the gated
+    kernels use) for every finite bf16 and fp16 value z, bit for bit against the
     oracle's; and the fast path's error, over every finite fp32 input it
     serves, within the window of the near-tie test."""
     import os
@@ -162,9 +162,9 @@ def test_gate_exact_over_every_dtype_value(tmp_path):
     f = [l.split() for l in res.splitlines() if l.startswith("silu")][0]
     v = {f[i]: int(f[i + 1]) for i in range(1, len(f) - 1, 2)}
     assert v["max_bits"] <= v["window"], res
-    gates = np.fromfile(out, np.uint16).reshape(3, 65536)
+    gates = np.fromfile(out, np.uint16).reshape(4, 65536)
     z = np.arange(65536, dtype=np.uint16)
-    for i, dt in enumerate(["bf16", "fp16", "bf16"]):  # the third: the bf16 table path
+    for i, dt in enumerate(["bf16", "fp16", "bf16", "fp16"]):  # then the two table paths
         finite = np.isfinite(pins.bits_to_f64(z, dt))
         ref = O.silu_dt(dt, z)
         bad = np.flatnonzero(finite & (gates[i] != ref))
