@@ -380,7 +380,8 @@ def measure_next_rows(wl, peak_kind_gbs, iters=50, evict=True):
     prefill / large NVFP4 workloads, the large NVFP4 call with its block
     scales in the swizzled GEMM layout (same bytes: 16,384 rows and 7168
     columns need no padding), the gated RMSNorm + NVFP4 call on the same
-    rows (the residual as the gate), the Q/K call storing K into a KV pool
+    rows (the residual as the gate; also with swizzled scales, and on fp16
+    inputs of the same recipe), the Q/K call storing K into a KV pool
     of 8192 slots at shuffled slot indices (uniform FP8 rows, and mixed rows
     of 64 FP8 codes + 64 bf16 rope values per head), and the Q/K call with
     dynamic scales (amax pass + fused pass)."""
@@ -408,7 +409,21 @@ def measure_next_rows(wl, peak_kind_gbs, iters=50, evict=True):
         # gated: read x and the gate z, write codes and scales (no residual, no norm out)
         ("gated_rmsnorm_nvfp4", NV_ROWS, NV_ROWS * NV_H * (4 + 0.5 + 1 / 16) + NV_H * 2 + 4,
          lambda: rq.rq_gated_rmsnorm_nvfp4(d["x5"], d["r5"], wl.w5, EPS, wl.gs5, wl.p5, wl.sf5)),
+        ("gated_rmsnorm_nvfp4_swizzled", NV_ROWS,
+         NV_ROWS * NV_H * (4 + 0.5 + 1 / 16) + NV_H * 2 + 4,
+         lambda: rq.rq_gated_rmsnorm_nvfp4_swizzled(d["x5"], d["r5"], wl.w5, EPS, wl.gs5, wl.p5,
+                                                    sf_swz)),
     ]
+    # the gated call on fp16 inputs of the same recipe (generated in fp16, not
+    # converted from the bf16 ones, whose low mantissa bits are all zero):
+    # 1024 generated rows repeated to the 16,384 rows of the call
+    hx, hz, hw = synth.rows_input(0, 1024, NV_H, "fp16", outlier_frac=0.01)
+    f16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.float16).cuda()
+    x16, z16 = (f16(a).repeat(NV_ROWS // 1024, 1) for a in (hx, hz))
+    w16 = f16(hw)
+    cases.append(("gated_rmsnorm_nvfp4_fp16", NV_ROWS,
+                  NV_ROWS * NV_H * (4 + 0.5 + 1 / 16) + NV_H * 2 + 4,
+                  lambda: rq.rq_gated_rmsnorm_nvfp4(x16, z16, w16, EPS, wl.gs5, wl.p5, wl.sf5)))
     n_slots = 2 * QK_T
     pool = torch.empty((n_slots, QK_HK, QK_D), dtype=torch.uint8, device="cuda")
     slots = torch.randperm(n_slots, generator=torch.Generator().manual_seed(0))[:QK_T].cuda()
