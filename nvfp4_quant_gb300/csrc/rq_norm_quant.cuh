@@ -36,6 +36,9 @@ struct GroupShape {
     static constexpr int kRowsPerCta = kBlock / G;
     static constexpr int kWarps = kBlock / 32;
     static constexpr int kWarpsPerGroup = G > 32 ? G / 32 : 1;
+    // per-warp partial sums in shared memory: a row of them per parity,
+    // padded to whole 16-byte vectors (the padding holds zeros)
+    static constexpr int kRedStride = (kWarps + 3) & ~3;
 };
 
 // Byte offset of the block scale of (row, block column c).  Linear layout:
@@ -124,7 +127,7 @@ __host__ __device__ constexpr int dynamic_smem_bytes()
 // kernel picks the body once; see Divisor).
 template <typename DT, int G, int VPT, int MODE, bool kFast>
 __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
-                                                       float (*red)[GroupShape<G>::kWarps])
+                                                       float (*red)[GroupShape<G>::kRedStride])
 {
     using S = GroupShape<G>;
     const int tid = threadIdx.x;
@@ -239,9 +242,23 @@ __device__ __forceinline__ void add_rmsnorm_quant_body(const NormQuantParams &p,
             if ((tid & 31) == 0) red[parity][tid >> 5] = ss;
             __syncthreads();
             const int w0 = grp * S::kWarpsPerGroup;
-            ss = 0.0f;
+            if constexpr (S::kWarpsPerGroup >= 8) {
+                // one row per CTA (w0 = 0): the partials as 16-byte vectors,
+                // added pairwise with packed adds (the padding adds +0)
+                const float4 *r4 = reinterpret_cast<const float4 *>(red[parity]);
+                float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
-            for (int i = 0; i < S::kWarpsPerGroup; ++i) ss = __fadd_rn(ss, red[parity][w0 + i]);
+                for (int i = 0; i < S::kRedStride / 4; ++i) {
+                    const float4 v = r4[i];
+                    acc = __fadd2_rn(acc, make_float2(v.x, v.y));
+                    acc = __fadd2_rn(acc, make_float2(v.z, v.w));
+                }
+                ss = __fadd_rn(acc.x, acc.y);
+            } else {
+                ss = 0.0f;
+#pragma unroll
+                for (int i = 0; i < S::kWarpsPerGroup; ++i) ss = __fadd_rn(ss, red[parity][w0 + i]);
+            }
             parity ^= 1;
         }
         const float ms = __fdiv_rn(ss, (float)p.hidden);
@@ -388,7 +405,12 @@ template <typename DT, int G, int VPT, int MODE>
 __global__ void __launch_bounds__(GroupShape<G>::kBlock, (min_ctas_per_sm<G, VPT>()))
 add_rmsnorm_quant_kernel(const NormQuantParams p)
 {
-    __shared__ float red[2][GroupShape<G>::kWarps];
+    using S = GroupShape<G>;
+    __shared__ __align__(16) float red[2][S::kRedStride];
+    if (S::kRedStride > S::kWarps && threadIdx.x < 2 * (S::kRedStride - S::kWarps)) {
+        const int pad = S::kRedStride - S::kWarps;  // never written by a warp's partial
+        red[threadIdx.x / pad][S::kWarps + threadIdx.x % pad] = 0.0f;
+    }
     pdl_trigger();
     if (MODE == MODE_FP8) pdl_wait();  // before the scale load; the body waits in any case
     if (MODE == MODE_FP8 && !Divisor(ld_f32(p.scale)).fast)
