@@ -143,6 +143,26 @@ def test_gate_saturates_and_handles_extreme_gates():
     check_gated("bf16", x, z, w, 1e-6, gated_gs("bf16", x, z, w, 1e-6))
 
 
+@pytest.mark.parametrize("dt", ["bf16", "fp16"])
+def test_gates_at_and_beyond_the_table_edges(dt):
+    # the 448 x 2 shape (more rows than SMs, 7168 elements), whose gates come
+    # from the shared-memory tables: gates on both sides of each table's
+    # edges (bf16 2^-23 and 512, fp16 32) and far beyond, mixed with N(0, 1)
+    # gates in the same vectors
+    rows, hidden = SMS + 48, 7168
+    x, z, w = synth.rows_input(12, rows, hidden, dt)
+    # (large enough to cross the edges, small enough that x * gate and the
+    # sum of squares stay finite)
+    edges = {"bf16": [2.0 ** -23, 2.0 ** -24, 2.0 ** -30, 508.0, 512.0, 1000.0, 3.0e4],
+             "fp16": [31.96875, 32.0, 33.0, 40.0, 1000.0, 2.0 ** -24, 6.0e-5]}[dt]
+    vals = np.array(edges + [-e for e in edges])
+    zf = pins.bits_to_f64(z, dt)
+    pick = (np.arange(rows * hidden).reshape(rows, hidden) * 7919) % 5 == 0
+    zf = np.where(pick, vals[(np.arange(rows * hidden).reshape(rows, hidden) // 5) % vals.size], zf)
+    z = pins.f64_to_dt(zf, dt)
+    check_gated(dt, x, z, w, 1e-6, gated_gs(dt, x, z, w, 1e-6))
+
+
 def test_gate_exact_over_every_dtype_value(tmp_path):
     """The kernel's gate dt(silu(z)) (tests/cuda/silu_check.cu runs the
     library's device code: the fast path with its exact path for both dtypes,
