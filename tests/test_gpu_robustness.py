@@ -11,6 +11,7 @@ import nvfp4_quant_gb300 as rq
 import oracle as O
 import synth
 from nvfp4_quant_gb300 import build as rq_build
+from tests import pins
 from tests.gpu_util import assert_codes, dev16, f32dev, host8, host16
 
 pytestmark = pytest.mark.gpu
@@ -252,3 +253,27 @@ def test_back_to_back_calls_see_each_others_writes():
                                       0.05)
     assert_codes(host8(qo).reshape(qq_ref.shape), qq_ref, 0x80, "Q codes after a row call")
     assert_codes(host8(ko).reshape(kq_ref.shape), kq_ref, 0x80, "K codes after a row call")
+
+
+def test_calls_around_other_kernels_see_their_writes():
+    """A library kernel after a kernel launched without dependent-launch
+    attributes (torch's) and before one: the library call reads what torch
+    wrote just before it, and torch reads what the library call wrote."""
+    rows, H = 2048, 4096
+    x, r, w = synth.rows_input(62, rows, H, "fp16")
+    xd, rd, wd = dev16(x, "fp16"), dev16(r, "fp16"), dev16(w, "fp16")
+    q = torch.empty((rows, H), dtype=torch.uint8, device="cuda")
+    sc = f32dev(0.04)
+    for _ in range(3):
+        rd.mul_(-1.0)  # torch writes the residual (exact: a sign flip)
+        rq.rq_add_rmsnorm_fp8(xd, rd, rd, wd, 1e-6, sc, q)  # reads it, writes r' in place
+        rd.mul_(0.5)  # torch reads r' right after (exact: a power of two)
+    torch.cuda.synchronize()
+    hr = r.copy()
+    for _ in range(3):
+        hr = pins.f64_to_dt(-pins.bits_to_f64(hr, "fp16"), "fp16")
+        s_ref, _, q_ref = O.add_rmsnorm_fp8("fp16", x, hr, w, 1e-6, 0.04)
+        hr = pins.f64_to_dt(0.5 * pins.bits_to_f64(s_ref, "fp16"), "fp16")
+    assert np.array_equal(host16(rd), hr)
+    assert_codes(host8(q), q_ref, 0x80, "FP8 codes of the last call")
+
