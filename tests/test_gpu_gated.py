@@ -196,7 +196,7 @@ def test_gate_exact_over_every_dtype_value(tmp_path):
 
 
 @pytest.mark.parametrize("rows,hidden,dt", [(130, 96, "bf16"), (300, 1056, "fp16"), (16384, 7168, "bf16"),
-                                            (-1, 16384, "bf16"), (5, 8208, "fp16")])
+                                            (1300, 7168, "fp16"), (-1, 16384, "bf16"), (5, 8208, "fp16")])
 def test_gated_swizzled_scales(rows, hidden, dt):
     """The swizzled gated call: codes equal to the linear call's, scales byte
     for byte the oracle's layout of the linear call's scales, padding zero
