@@ -424,17 +424,53 @@ def rq_nvfp4_swizzled_scale_bytes(rows, hidden):
 
 
 # ---------------------------------------------------------------- conveniences
+def _nvfp4_outputs(x, rows, hidden, swizzled):
+    q = torch.empty((rows, hidden // 2), dtype=torch.uint8, device=x.device)
+    if swizzled:
+        sf = torch.empty((rq_nvfp4_swizzled_scale_bytes(rows, hidden),), dtype=torch.uint8,
+                         device=x.device)
+    else:
+        sf = torch.empty((rows, hidden // 16), dtype=torch.uint8, device=x.device)
+    return q, sf
+
+
 def add_rmsnorm_nvfp4(x, residual, weight, eps, global_scale, with_norm_out=False,
-                      in_place=True, stream=None):
-    """Allocate the outputs (torch) and run rq_add_rmsnorm_nvfp4.  Returns
-    (residual_out, q_packed, block_scales, norm_out or None)."""
+                      in_place=True, swizzled=False, stream=None):
+    """Allocate the outputs (torch) and run rq_add_rmsnorm_nvfp4 (or, with
+    swizzled, rq_add_rmsnorm_nvfp4_swizzled: block_scales then is the flat
+    buffer in the GEMM's tile layout).  Returns (residual_out, q_packed,
+    block_scales, norm_out or None)."""
     rows, hidden = _rows(x, residual)
     res_out = residual if in_place else torch.empty_like(x)
-    q = torch.empty((rows, hidden // 2), dtype=torch.uint8, device=x.device)
-    sf = torch.empty((rows, hidden // 16), dtype=torch.uint8, device=x.device)
+    q, sf = _nvfp4_outputs(x, rows, hidden, swizzled)
     y = torch.empty_like(x) if with_norm_out else None
-    rq_add_rmsnorm_nvfp4(x, residual, res_out, weight, eps, global_scale, q, sf, y, stream)
+    call = rq_add_rmsnorm_nvfp4_swizzled if swizzled else rq_add_rmsnorm_nvfp4
+    call(x, residual, res_out, weight, eps, global_scale, q, sf, y, stream)
     return res_out, q, sf, y
+
+
+def gated_rmsnorm_nvfp4(x, z, weight, eps, global_scale, with_norm_out=False, swizzled=False,
+                        stream=None):
+    """Allocate the outputs (torch) and run rq_gated_rmsnorm_nvfp4 (or its
+    swizzled form).  Returns (q_packed, block_scales, norm_out or None)."""
+    rows, hidden = _rows(x, z)
+    q, sf = _nvfp4_outputs(x, rows, hidden, swizzled)
+    y = torch.empty_like(x) if with_norm_out else None
+    call = rq_gated_rmsnorm_nvfp4_swizzled if swizzled else rq_gated_rmsnorm_nvfp4
+    call(x, z, weight, eps, global_scale, q, sf, y, stream)
+    return q, sf, y
+
+
+def qk_rmsnorm_rope_fp8(q, k, q_weight, k_weight, eps, positions, cos_sin_cache, q_scale,
+                        k_scale, stream=None):
+    """Allocate dense FP8 outputs (torch) and run rq_qk_rmsnorm_rope_fp8.
+    Returns (q_out [T, Hq, 128], k_out [T, Hk, 128]); either is None when its
+    input is None."""
+    q_out = None if q is None else torch.empty(tuple(q.shape), dtype=torch.uint8, device=q.device)
+    k_out = None if k is None else torch.empty(tuple(k.shape), dtype=torch.uint8, device=k.device)
+    rq_qk_rmsnorm_rope_fp8(q, k, q_weight, k_weight, eps, positions, cos_sin_cache, q_scale,
+                           k_scale, q_out, k_out, stream)
+    return q_out, k_out
 
 
 def add_rmsnorm_fp8(x, residual, weight, eps, scale, with_norm_out=False, in_place=True,

@@ -277,3 +277,38 @@ def test_calls_around_other_kernels_see_their_writes():
     assert np.array_equal(host16(rd), hr)
     assert_codes(host8(q), q_ref, 0x80, "FP8 codes of the last call")
 
+
+
+def test_allocating_conveniences_match_the_explicit_calls():
+    """The allocating Python conveniences give the explicit calls' outputs."""
+    rows, H = 300, 2048
+    x, r, w = synth.rows_input(63, rows, H, "bf16")
+    xd, wd = dev16(x, "bf16"), dev16(w, "bf16")
+    gs = f32dev(300.0)
+    u8 = lambda *s: torch.empty(s, dtype=torch.uint8, device="cuda")
+    for swz in (False, True):
+        rd = dev16(r, "bf16")
+        ro, q, sf, y = rq.add_rmsnorm_nvfp4(xd, rd, wd, 1e-6, gs, with_norm_out=True,
+                                            in_place=False, swizzled=swz)
+        q2, y2 = u8(rows, H // 2), torch.empty_like(xd)
+        sf2 = u8(rq.rq_nvfp4_swizzled_scale_bytes(rows, H)) if swz else u8(rows, H // 16)
+        ro2 = torch.empty_like(xd)
+        (rq.rq_add_rmsnorm_nvfp4_swizzled if swz else rq.rq_add_rmsnorm_nvfp4)(
+            xd, rd, ro2, wd, 1e-6, gs, q2, sf2, y2)
+        torch.cuda.synchronize()
+        assert all(torch.equal(a, b) for a, b in ((ro, ro2), (q, q2), (sf, sf2), (y, y2)))
+        zd = dev16(r, "bf16")
+        q, sf, y = rq.gated_rmsnorm_nvfp4(xd, zd, wd, 1e-6, gs, with_norm_out=True, swizzled=swz)
+        (rq.rq_gated_rmsnorm_nvfp4_swizzled if swz else rq.rq_gated_rmsnorm_nvfp4)(
+            xd, zd, wd, 1e-6, gs, q2, sf2, y2)
+        torch.cuda.synchronize()
+        assert all(torch.equal(a, b) for a, b in ((q, q2), (sf, sf2), (y, y2)))
+    T, Hq, Hk, D = 100, 4, 2, 128
+    qh, kh, qw, kw, pos, cs = synth.qk_input(64, T, Hq, Hk, D, "bf16")
+    args = (dev16(qh, "bf16"), dev16(kh, "bf16"), dev16(qw, "bf16"), dev16(kw, "bf16"), 1e-6,
+            torch.from_numpy(pos).cuda(), torch.from_numpy(cs).cuda(), f32dev(0.02), f32dev(0.03))
+    qo, ko = rq.qk_rmsnorm_rope_fp8(*args)
+    qo2, ko2 = u8(T, Hq, D), u8(T, Hk, D)
+    rq.rq_qk_rmsnorm_rope_fp8(*args, qo2, ko2)
+    torch.cuda.synchronize()
+    assert qo.shape == (T, Hq, D) and torch.equal(qo, qo2) and torch.equal(ko, ko2)
