@@ -68,7 +68,7 @@ typedef enum {
 /* Storage type of x, residual, weight and norm_out (all must match). */
 typedef enum { RQ_BF16 = 0, RQ_FP16 = 1 } rq_dtype;
 
-#define RQ_MAX_HIDDEN 32768
+#define RQ_MAX_HIDDEN 262144
 #define RQ_QK_HEAD_DIM 128
 #define RQ_QK_MAX_HEADS 65536
 

@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "lib", "librq.so")
 
 RQ_BF16, RQ_FP16 = 0, 1
-RQ_MAX_HIDDEN = 32768
+RQ_MAX_HIDDEN = 262144
 RQ_QK_HEAD_DIM = 128
 RQ_QK_MAX_HEADS = 65536
 STATUS = {0: "RQ_OK", 1: "RQ_ERR_NULL", 2: "RQ_ERR_SHAPE", 3: "RQ_ERR_DTYPE",

@@ -5,6 +5,7 @@
 #include <atomic>
 
 #include "rq_norm_quant.cuh"
+#include "rq_norm_quant_long.cuh"
 #include "rq_norm_quant_staged.cuh"
 #include "rq.h"
 
@@ -65,7 +66,7 @@ static cudaError_t launch_staged(const NormQuantParams &p, cudaStream_t stream)
     const int d = dev < kMaxDevices ? dev : 0;
     if (!attr_set[d].load(std::memory_order_relaxed)) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 32 * (RQ_MAX_HIDDEN / 8));
+                                 32 * kStagedMaxNvec);
         if (e != cudaSuccess) return e;
         attr_set[d].store(1, std::memory_order_relaxed);
     }
@@ -82,6 +83,21 @@ static cudaError_t launch_staged(const NormQuantParams &p, cudaStream_t stream)
     return launch_pdl(kern, grid, kStagedThreads, smem, stream, p);
 }
 
+// Rows above 32768 elements: one CTA of kLongThreads per row, persistent grid.
+template <typename DT, int MODE>
+static cudaError_t launch_long(const NormQuantParams &p, cudaStream_t stream)
+{
+    static std::atomic<int> occ_cache[kMaxDevices];
+    auto kern = add_rmsnorm_quant_long_kernel<DT, MODE>;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const int per_sm = resident_ctas(kern, kLongThreads, dev, occ_cache);
+    const int64_t full = (int64_t)device_sms(dev) * per_sm;
+    const int grid = (int)(p.rows < full ? p.rows : full);
+    return launch_pdl(kern, grid, kLongThreads, 0, stream, p);
+}
+
 // Thread-group shape by row length (nvec 16-byte vectors per row): with at
 // most one row per SM, a wide group (256 or 512 threads per row); otherwise
 // the smallest listed G x VPT that covers the row.  Rows above 8192 elements go
@@ -95,6 +111,7 @@ cudaError_t launch_add_rmsnorm(const NormQuantParams &p, cudaStream_t stream)
 {
     const int n = p.nvec;
     int dev = 0;
+    if (n > 4096) return launch_long<DT, MODE>(p, stream);  // hidden above 32768
     // At most one row per SM: one CTA per row either way, so give each row
     // more threads and each thread fewer vectors (a shorter serial chain per
     // thread; measured on GB300 in a CUDA graph, the [64, 8192] fp16 NVFP4

@@ -21,6 +21,9 @@
 namespace rq {
 
 constexpr int kStagedThreads = 256;
+// the longest row (in 16-byte vectors) the kernel's dynamic shared memory is
+// allowed for: 32 bytes per vector (x and residual), 128 KB
+constexpr int kStagedMaxNvec = 4096;
 
 template <typename DT, int MODE, bool kFast>
 __device__ __forceinline__ void staged_body(const NormQuantParams &p, uint4 *buf, float (*red)[kStagedThreads / 32])

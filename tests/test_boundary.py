@@ -96,7 +96,7 @@ def test_row_call_rejections(L, call):
     assert call(L, rows=0, dt=7) == DTYPE
     assert call(L, hidden=0) == SHAPE
     assert call(L, hidden=136) == SHAPE  # not a multiple of 16
-    assert call(L, hidden=32768 + 16) == UNSUP
+    assert call(L, hidden=rq.RQ_MAX_HIDDEN + 16) == UNSUP
     assert call(L, dt=2) == DTYPE
     assert call(L, x=A["x"] + 8) == MISAL
     assert call(L, q=A["q"] + 4) == MISAL

@@ -60,7 +60,7 @@ def test_per_token_fp8(hidden, dt):
     assert np.all(rel <= 2.0 ** -7)
 
 
-@pytest.mark.parametrize("hidden", [256, 7168])
+@pytest.mark.parametrize("hidden", [256, 7168, 40976])
 @pytest.mark.parametrize("dt", ["bf16", "fp16"])
 @pytest.mark.parametrize("in_place", [False, True])
 def test_dynamic_tensor_fp8_and_nvfp4(hidden, dt, in_place):

@@ -73,7 +73,7 @@ def test_gated_16384x7168_bf16():
     check_gated("bf16", x, z, w, 1e-6, gated_gs("bf16", x, z, w, 1e-6))
 
 
-HIDDEN = [16, 48, 128, 144, 512, 1040, 2064, 4096, 4112, 6016, 7168, 8208, 16384, 32768]
+HIDDEN = [16, 48, 128, 144, 512, 1040, 2064, 4096, 4112, 6016, 7168, 8208, 16384, 32768, 40976]
 
 
 @pytest.mark.parametrize("hidden", HIDDEN)

@@ -5,6 +5,7 @@ import pytest
 import torch
 
 import nvfp4_quant_gb300 as rq
+from nvfp4_quant_gb300 import RQ_MAX_HIDDEN
 import oracle as O
 import synth
 from nvfp4_quant_gb300 import build as rq_build
@@ -324,6 +325,36 @@ def test_long_rows_through_shared_memory(hidden, dt):
     amax calibration against the oracle."""
     rows = 2 * SMS + 3
     x, r, w = synth.rows_input(hidden + 7, rows, hidden, dt, res_std=2.0, outlier_frac=0.01)
+    gs, scale = oracle_gs(dt, x, r, w, 1e-6)
+    check_fp8(dt, x, r, w, 1e-6, scale, norm_out=True)
+    check_nvfp4(dt, x, r, w, 1e-6, gs, norm_out=True, in_place=True)
+    _, y_ref = O.add_rmsnorm(dt, x, r, w, 1e-6)
+    xd, rd, wd = dev16(x, dt), dev16(r, dt), dev16(w, dt)
+    q = torch.empty((rows, hidden), dtype=torch.uint8, device="cuda")
+    sc = torch.empty(rows, dtype=torch.float32, device="cuda")
+    y = torch.empty_like(xd)
+    rq.rq_add_rmsnorm_fp8_per_token(xd, rd, torch.empty_like(rd), wd, 1e-6, q, sc, y)
+    amax = f32dev(0.0)
+    rq.rq_add_rmsnorm_amax(xd, rd, wd, 1e-6, amax)
+    torch.cuda.synchronize()
+    q_o, sc_o = O.quant_fp8_per_row(dt, host16(y))
+    assert np.array_equal(host8(q), q_o) and np.array_equal(sc.cpu().numpy(), sc_o)
+    assert_norm_within_ulp(host16(y), y_ref, dt)
+    a_ref = O.amax(dt, y_ref)
+    assert abs(float(amax.item()) - a_ref) <= pins.ulp(np.array([a_ref]), dt)[0]
+
+
+# ------------------------------------------------------------- rows above 32768
+@pytest.mark.parametrize("hidden,rows", [(32784, -2), (40976, 5), (65536, -1), (RQ_MAX_HIDDEN, 3)])
+@pytest.mark.parametrize("dt", ["bf16", "fp16"])
+def test_rows_beyond_the_register_shapes(hidden, rows, dt):
+    """Rows above 32768 elements run the two-pass kernel (one CTA per row,
+    residual' read back from where pass 1 stored it): FP8, NVFP4 with norm
+    out, per-token FP8 and the amax calibration against the oracle.  Row
+    counts -1 / -2: the SM count + 1 / twice it + 3 (past the persistent
+    grid)."""
+    rows = {-1: SMS + 1, -2: 2 * SMS + 3}.get(rows, rows)
+    x, r, w = synth.rows_input(hidden + 9, rows, hidden, dt, res_std=2.0, outlier_frac=0.01)
     gs, scale = oracle_gs(dt, x, r, w, 1e-6)
     check_fp8(dt, x, r, w, 1e-6, scale, norm_out=True)
     check_nvfp4(dt, x, r, w, 1e-6, gs, norm_out=True, in_place=True)

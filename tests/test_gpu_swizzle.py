@@ -164,7 +164,9 @@ CASES = [(1, 16, "bf16"), (127, 48, "fp16"), (129, 80, "bf16"), (130, 96, "bf16"
          (300, 1056, "fp16"), (257, 7168, "bf16"), (STAGED, 8208, "bf16"),
          (STAGED, 16384, "fp16"), (3, 32768, "bf16"),
          # several rows per CTA, and a ragged last tile of 128 rows
-         (2000, 7168, "bf16"), (3700, 4096, "fp16")]
+         (2000, 7168, "bf16"), (3700, 4096, "fp16"),
+         # rows above 32768 elements (the two-pass kernel)
+         (5, 40976, "bf16"), (130, 65536, "fp16")]
 
 
 @pytest.mark.parametrize("rows,hidden,dt", CASES)
