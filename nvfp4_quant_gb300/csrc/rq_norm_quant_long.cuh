@@ -21,6 +21,7 @@
 namespace rq {
 
 constexpr int kLongThreads = 512;
+constexpr int kLongUnroll = 2;  // vectors per thread whose loads are issued together
 
 template <typename DT, int MODE, bool kFast>
 __device__ __forceinline__ void long_body(const NormQuantParams &p, float (*red)[kLongThreads / 32])
@@ -42,11 +43,12 @@ __device__ __forceinline__ void long_body(const NormQuantParams &p, float (*red)
     float amax_acc = 0.0f;
     int parity = 0;
 
-    // residual' (or g) of vector k of a row, from the inputs
-    auto form = [&](int64_t row, int k) {
-        const int64_t off = (row * H + (int64_t)k * 8) * 2;
-        const uint4 xv = ld_stream16(static_cast<const uint8_t *>(p.x) + off);
-        const uint4 rv = ld_stream16(static_cast<const uint8_t *>(p.res_in) + off);
+    constexpr int U = kLongUnroll;
+    const uint8_t *px = static_cast<const uint8_t *>(p.x);
+    const uint8_t *pr = static_cast<const uint8_t *>(p.res_in);
+    auto at = [&](int64_t row, int k) { return (row * H + (int64_t)k * 8) * 2; };
+    // residual' (or g) from the loaded x and residual (gate) vectors
+    auto form = [&](uint4 xv, uint4 rv) {
         if (is_gated<MODE>()) return mul8<DT>(xv, silu_gate8<DT>(rv));
         float a[8], b[8];
         unpack8<DT>(xv, a);
@@ -55,11 +57,26 @@ __device__ __forceinline__ void long_body(const NormQuantParams &p, float (*red)
         for (int e = 0; e < 8; ++e) a[e] = __fadd_rn(a[e], b[e]);
         return pack8<DT>(a);
     };
-    // pass 2 and 3: the value pass 1 formed, read back or formed again
-    auto again = [&](int64_t row, int k) {
-        if (kWrites)
-            return ld_stream16(static_cast<const uint8_t *>(p.res_out) + (row * H + (int64_t)k * 8) * 2);
-        return form(row, k);
+    // pass 2 and 3: the values pass 1 formed for vectors i0 .. i0 + U - 1 of
+    // this thread, read back or formed again (the loads of all U first)
+    auto again = [&](int64_t row, int i0, uint4 (&sv)[U]) {
+        uint4 xv[U], rv[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int k = (i0 + u) * T + tid;
+            const bool ok = i0 + u < iters && k < nvec;
+            if (kWrites) {
+                sv[u] = ok ? ld_stream16(static_cast<const uint8_t *>(p.res_out) + at(row, k))
+                           : make_uint4(0, 0, 0, 0);
+            } else {
+                xv[u] = ok ? ld_stream16(px + at(row, k)) : make_uint4(0, 0, 0, 0);
+                rv[u] = ok ? ld_stream16(pr + at(row, k)) : make_uint4(0, 0, 0, 0);
+            }
+        }
+        if (!kWrites) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) sv[u] = form(xv[u], rv[u]);
+        }
     };
     // y = dt((s * rstd) * w) of vector k
     auto norm = [&](uint4 sv, int k, float rstd, float (&y)[8]) {
@@ -72,17 +89,29 @@ __device__ __forceinline__ void long_body(const NormQuantParams &p, float (*red)
     };
 
     for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
-        // ---- pass 1: residual' (stored), its squares
+        // ---- pass 1: residual' (stored), its squares; the loads of U
+        // vectors first (the stores go to other addresses than these loads)
         float ss = 0.0f;
-        for (int i = 0; i < iters; ++i) {
-            const int k = i * T + tid;
-            if (k < nvec) {
-                const uint4 sv = form(row, k);
-                if (kWrites) st16(static_cast<uint8_t *>(p.res_out) + (row * H + (int64_t)k * 8) * 2, sv);
-                float a[8];
-                unpack8<DT>(sv, a);
+        for (int i0 = 0; i0 < iters; i0 += U) {
+            uint4 xv[U], rv[U];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) ss = __fmaf_rn(a[e], a[e], ss);  // squares are exact
+            for (int u = 0; u < U; ++u) {
+                const int k = (i0 + u) * T + tid;
+                const bool ok = i0 + u < iters && k < nvec;
+                xv[u] = ok ? ld_stream16(px + at(row, k)) : make_uint4(0, 0, 0, 0);
+                rv[u] = ok ? ld_stream16(pr + at(row, k)) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int k = (i0 + u) * T + tid;
+                if (i0 + u < iters && k < nvec) {
+                    const uint4 sv = form(xv[u], rv[u]);
+                    if (kWrites) st16(static_cast<uint8_t *>(p.res_out) + at(row, k), sv);
+                    float a[8];
+                    unpack8<DT>(sv, a);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) ss = __fmaf_rn(a[e], a[e], ss);  // squares are exact
+                }
             }
         }
         ss = group_sum<32>(ss);
@@ -97,41 +126,47 @@ __device__ __forceinline__ void long_body(const NormQuantParams &p, float (*red)
 
         // ---- pass 2: normalise, store, quantise
         float row_amax = 0.0f;
-        for (int i = 0; i < iters; ++i) {
-            const int k = i * T + tid;
-            const bool ok = k < nvec;
-            float y[8];
-            uint4 yv = make_uint4(0, 0, 0, 0);
-            if (ok) yv = norm(again(row, k), k, rstd, y);
-            if (MODE != MODE_AMAX && p.norm_out != nullptr && ok)
-                st16(static_cast<uint8_t *>(p.norm_out) + (row * H + (int64_t)k * 8) * 2, yv);
-            unpack8<DT>(yv, y);  // quantise from the dtype-rounded norm output
-            if (MODE == MODE_FP8) {
-                float v[8];
+        for (int i0 = 0; i0 < iters; i0 += U) {
+            uint4 sv[U];
+            again(row, i0, sv);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = div_by<kFast>(y[e], by_scale);
-                const uint2 c = e4m3x8(v);
-                if (ok) st8(p.q + row * H + (int64_t)k * 8, c.x, c.y);
-            } else if (is_nvfp4<MODE>()) {
-                float m = 0.0f;
+            for (int u = 0; u < U; ++u) {
+                if (i0 + u >= iters) break;  // the same for every thread
+                const int k = (i0 + u) * T + tid;
+                const bool ok = k < nvec;
+                float y[8];
+                uint4 yv = make_uint4(0, 0, 0, 0);
+                if (ok) yv = norm(sv[u], k, rstd, y);
+                if (MODE != MODE_AMAX && p.norm_out != nullptr && ok)
+                    st16(static_cast<uint8_t *>(p.norm_out) + at(row, k), yv);
+                unpack8<DT>(yv, y);  // quantise from the dtype-rounded norm output
+                if (MODE == MODE_FP8) {
+                    float v[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(y[e]));
-                const float a = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));  // 16-element block
-                const float t2 = div_by<true>(__fmul_rn(scale, a), by_six);
-                const uint32_t sfc = e4m3x2(t2, 0.0f) & 0xFFu;
-                const float sfv = e4m3_value(sfc);
-                const float enc = sfv == 0.0f ? 0.0f : __fdiv_rn(scale, sfv);
-                float v[8];
+                    for (int e = 0; e < 8; ++e) v[e] = div_by<kFast>(y[e], by_scale);
+                    const uint2 c = e4m3x8(v);
+                    if (ok) st8(p.q + row * H + (int64_t)k * 8, c.x, c.y);
+                } else if (is_nvfp4<MODE>()) {
+                    float m = 0.0f;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(y[e], enc);
-                const uint32_t codes = e2m1x8(v);
-                if (ok) st4(p.q + row * (H / 2) + (int64_t)k * 4, codes);
-                store_block_scale<is_swizzled<MODE>()>(p, row, k, ok, sfc, sf_words);
-            } else if (ok) {  // per-token FP8 (its row maximum first) or amax
+                    for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(y[e]));
+                    const float a = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));  // 16-element block
+                    const float t2 = div_by<true>(__fmul_rn(scale, a), by_six);
+                    const uint32_t sfc = e4m3x2(t2, 0.0f) & 0xFFu;
+                    const float sfv = e4m3_value(sfc);
+                    const float enc = sfv == 0.0f ? 0.0f : __fdiv_rn(scale, sfv);
+                    float v[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    if (MODE == MODE_FP8_ROW) row_amax = fmaxf(row_amax, fabsf(y[e]));
-                    else amax_acc = fmaxf(amax_acc, fabsf(y[e]));
+                    for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(y[e], enc);
+                    const uint32_t codes = e2m1x8(v);
+                    if (ok) st4(p.q + row * (H / 2) + (int64_t)k * 4, codes);
+                    store_block_scale<is_swizzled<MODE>()>(p, row, k, ok, sfc, sf_words);
+                } else if (ok) {  // per-token FP8 (its row maximum first) or amax
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        if (MODE == MODE_FP8_ROW) row_amax = fmaxf(row_amax, fabsf(y[e]));
+                        else amax_acc = fmaxf(amax_acc, fabsf(y[e]));
+                    }
                 }
             }
         }
@@ -149,20 +184,25 @@ __device__ __forceinline__ void long_body(const NormQuantParams &p, float (*red)
             const float rsc = row_amax > 0.0f ? div_rn(row_amax, 448.0f) : 1.0f;
             const Divisor d(rsc);
             if (tid == 0) p.row_scales[row] = rsc;
-            for (int i = 0; i < iters; ++i) {
-                const int k = i * T + tid;
-                if (k < nvec) {
-                    float y[8], v[8];
-                    unpack8<DT>(norm(again(row, k), k, rstd, y), y);
-                    if (d.fast) {
+            for (int i0 = 0; i0 < iters; i0 += U) {
+                uint4 sv[U];
+                again(row, i0, sv);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) v[e] = div_by<true>(y[e], d);
-                    } else {
+                for (int u = 0; u < U; ++u) {
+                    const int k = (i0 + u) * T + tid;
+                    if (i0 + u < iters && k < nvec) {
+                        float y[8], v[8];
+                        unpack8<DT>(norm(sv[u], k, rstd, y), y);
+                        if (d.fast) {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) v[e] = div_by<false>(y[e], d);
+                            for (int e = 0; e < 8; ++e) v[e] = div_by<true>(y[e], d);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) v[e] = div_by<false>(y[e], d);
+                        }
+                        const uint2 c = e4m3x8(v);
+                        st8(p.q + row * H + (int64_t)k * 8, c.x, c.y);
                     }
-                    const uint2 c = e4m3x8(v);
-                    st8(p.q + row * H + (int64_t)k * 8, c.x, c.y);
                 }
             }
         }
