@@ -660,6 +660,7 @@ def load_traffic(kernel):
 _ROW_SOURCES = ["include/rq.h", "nvfp4_quant_gb300/csrc/rq_launch.h",
                 "nvfp4_quant_gb300/csrc/rq_device.cuh", "nvfp4_quant_gb300/csrc/rq_norm_quant.cuh",
                 "nvfp4_quant_gb300/csrc/rq_norm_quant_staged.cuh",
+                "nvfp4_quant_gb300/csrc/rq_norm_quant_long.cuh",
                 "nvfp4_quant_gb300/csrc/rq_norm_quant_launch.cuh",
                 "nvfp4_quant_gb300/csrc/rq_norm_quant_bf16.cu"]
 _QK_SOURCES = ["include/rq.h", "nvfp4_quant_gb300/csrc/rq_launch.h",

@@ -100,12 +100,14 @@ static cudaError_t launch_long(const NormQuantParams &p, cudaStream_t stream)
 
 // Thread-group shape by row length (nvec 16-byte vectors per row): with at
 // most one row per SM, a wide group (256 or 512 threads per row); otherwise
-// the smallest listed G x VPT that covers the row.  Rows above 8192 elements go
-// through shared memory while two such CTAs fit per SM (up to 28672 elements:
-// 112 KB each) and there are at least two rows per SM; measured on GB300,
-// 16384 / 16400 / 20480-element rows ran at 0.82 / 0.79 / 0.74 of the copy
-// bandwidth staged against 0.75 / 0.57 / 0.67 register-resident, while at
-// 32768 (one CTA per SM) and with few rows the register-resident shapes win.
+// the smallest listed G x VPT that covers the row.  Rows of 8200 to 16384
+// elements go through shared memory when there are at least two rows per SM
+// (16384-element rows: 0.82 of the copy bandwidth staged against 0.75
+// register-resident).  Longer rows with more rows than SMs, and all rows above
+// 32768, take the two-pass kernel (rq_norm_quant_long.cuh), which beat both
+// on GB300: 1024 x 20480 NVFP4 with norm out 38.3 us against 46.7 staged,
+// 1000 x 24576 43.0 against 54.8, 2048 x 32768 100.8 against 106.0 for 512 x 8.
+// With at most one row per SM the wide register shapes stay faster.
 template <typename DT, int MODE>
 cudaError_t launch_add_rmsnorm(const NormQuantParams &p, cudaStream_t stream)
 {
@@ -135,14 +137,14 @@ cudaError_t launch_add_rmsnorm(const NormQuantParams &p, cudaStream_t stream)
     if (n <= 128) return launch_cfg<DT, 32, 4, MODE>(p, stream);
     if (n <= 256) return launch_cfg<DT, 64, 4, MODE>(p, stream);
     if (n <= 512) return launch_cfg<DT, 128, 4, MODE>(p, stream);
-    if (n > 1024 && n <= 3584) {
+    if (n > 1024 && n <= 2048) {
         if (cudaGetDevice(&dev) == cudaSuccess && p.rows >= 2 * (int64_t)device_sms(dev))
             return launch_staged<DT, MODE>(p, stream);
     }
     if (n <= 896) return launch_cfg<DT, 128, 7, MODE>(p, stream);
     if (n <= 1024) return launch_cfg<DT, 128, 8, MODE>(p, stream);
     if (n <= 2048) return launch_cfg<DT, 256, 8, MODE>(p, stream);
-    return launch_cfg<DT, 512, 8, MODE>(p, stream);  // n <= 4096 (hidden <= 32768)
+    return launch_long<DT, MODE>(p, stream);  // above 16384 elements
 }
 
 }  // namespace rq

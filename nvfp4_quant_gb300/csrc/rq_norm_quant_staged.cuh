@@ -1,5 +1,6 @@
 // rq_norm_quant_staged.cuh -- the fused residual add + RMSNorm + quant
-// kernel for long rows (hidden above 8192), staged through shared memory.
+// kernel for long rows (hidden 8200 to 16384, at least two rows per SM),
+// staged through shared memory.
 //
 // Register-resident rows of this length need 64 KB and more of registers per
 // row: one CTA per SM at most, or spills.  Here a CTA of kStagedThreads
@@ -22,8 +23,8 @@ namespace rq {
 
 constexpr int kStagedThreads = 256;
 // the longest row (in 16-byte vectors) the kernel's dynamic shared memory is
-// allowed for: 32 bytes per vector (x and residual), 128 KB
-constexpr int kStagedMaxNvec = 4096;
+// allowed for: 32 bytes per vector (x and residual), 64 KB
+constexpr int kStagedMaxNvec = 2048;
 
 template <typename DT, int MODE, bool kFast>
 __device__ __forceinline__ void staged_body(const NormQuantParams &p, uint4 *buf, float (*red)[kStagedThreads / 32])

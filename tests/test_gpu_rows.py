@@ -316,13 +316,14 @@ def test_fp8_codes_exact_for_every_value_at_many_scales(dt):
             assert np.array_equal(q, q_ref), "E4M3 codes differ at scale %r" % float(scale)
 
 
-# ------------------------------------------------------------- long rows (shared-memory staged)
+# ------------------------------------------------------------- long rows (staged / two-pass)
 @pytest.mark.parametrize("hidden", [8208, 16384, 16400, 20480, 28672])
 @pytest.mark.parametrize("dt", ["bf16", "fp16"])
 def test_long_rows_through_shared_memory(hidden, dt):
-    """Rows above 8192 elements, at least two per SM, run the kernel that
-    stages x and residual in shared memory: FP8, NVFP4, per-token FP8 and the
-    amax calibration against the oracle."""
+    """Rows above 8192 elements, at least two per SM: up to 16384 elements
+    the kernel that stages x and residual in shared memory, above it the
+    two-pass kernel.  FP8, NVFP4, per-token FP8 and the amax calibration
+    against the oracle."""
     rows = 2 * SMS + 3
     x, r, w = synth.rows_input(hidden + 7, rows, hidden, dt, res_std=2.0, outlier_frac=0.01)
     gs, scale = oracle_gs(dt, x, r, w, 1e-6)
