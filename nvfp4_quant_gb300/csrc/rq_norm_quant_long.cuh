@@ -24,7 +24,8 @@ constexpr int kLongThreads = 512;
 constexpr int kLongUnroll = 2;  // vectors per thread whose loads are issued together
 
 template <typename DT, int MODE, bool kFast>
-__device__ __forceinline__ void long_body(const NormQuantParams &p, float (*red)[kLongThreads / 32])
+__device__ __forceinline__ void long_body(const NormQuantParams &p, float (*red)[kLongThreads / 32],
+                                          const uint16_t *gtab)
 {
     constexpr int T = kLongThreads;
     constexpr int kWarps = T / 32;
@@ -49,7 +50,8 @@ __device__ __forceinline__ void long_body(const NormQuantParams &p, float (*red)
     auto at = [&](int64_t row, int k) { return (row * H + (int64_t)k * 8) * 2; };
     // residual' (or g) from the loaded x and residual (gate) vectors
     auto form = [&](uint4 xv, uint4 rv) {
-        if (is_gated<MODE>()) return mul8<DT>(xv, silu_gate8<DT>(rv));
+        if (is_gated<MODE>())  // bf16: the gate table (filled by the kernel)
+            return mul8<DT>(xv, std::is_same<DT, BF16>::value ? gate8_bf16(rv, gtab) : silu_gate8<DT>(rv));
         float a[8], b[8];
         unpack8<DT>(xv, a);
         unpack8<DT>(rv, b);
@@ -228,12 +230,19 @@ __global__ void __launch_bounds__(kLongThreads)
 add_rmsnorm_quant_long_kernel(const NormQuantParams p)
 {
     __shared__ float red[2][kLongThreads / 32];
+    // gated bf16: the gate table, filled before the wait (no global access)
+    constexpr bool kGateTab = is_gated<MODE>() && std::is_same<DT, BF16>::value;
+    __shared__ __align__(16) uint16_t gtab[kGateTab ? 2 * kGateHalf : 8];
     pdl_trigger();
+    if (kGateTab) {
+        gate_table_fill(gtab);
+        __syncthreads();
+    }
     pdl_wait();
     if (MODE == MODE_FP8 && !Divisor(ld_f32(p.scale)).fast)
-        long_body<DT, MODE, false>(p, red);
+        long_body<DT, MODE, false>(p, red, gtab);
     else
-        long_body<DT, MODE, true>(p, red);
+        long_body<DT, MODE, true>(p, red, gtab);
 }
 
 }  // namespace rq
