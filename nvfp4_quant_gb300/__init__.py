@@ -110,7 +110,13 @@ def _dt(t):
 
 
 def _ptr(t):
-    return None if t is None else t.data_ptr()
+    """Device pointer of a CUDA tensor (None for None).  A host tensor is
+    refused here: its address would reach the kernels as a device pointer."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("every tensor argument must be a CUDA tensor (got one on %s)" % t.device)
+    return t.data_ptr()
 
 
 def _stream(stream):

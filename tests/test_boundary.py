@@ -195,6 +195,20 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
         rq.lib()
 
 
+def test_binding_refuses_host_tensors(L):
+    """The Python binding passes device pointers only: a tensor in host
+    memory raises before any library call."""
+    import torch
+    x = torch.zeros((4, 64), dtype=torch.bfloat16)
+    w = torch.ones(64, dtype=torch.bfloat16)
+    s = torch.ones(1, dtype=torch.float32)
+    q = torch.empty((4, 64), dtype=torch.uint8)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        rq.rq_add_rmsnorm_fp8(x, x.clone(), torch.empty_like(x), w, 1e-6, s, q)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        rq.add_rmsnorm_nvfp4(x, x.clone(), w, 1e-6, s)
+
+
 def test_dynamic_rejections(L):
     pt = lambda **kw: L.rq_add_rmsnorm_fp8_per_token(
         kw.get("x", A["x"]), kw.get("r", A["r"]), kw.get("ro", A["ro"]), kw.get("w", A["w"]), 1e-6,
