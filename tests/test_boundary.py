@@ -34,6 +34,13 @@ def test_every_declared_symbol_is_exported(L):
         assert n in rq.SIGNATURES, "binding lacks " + n
 
 
+def test_binding_constants_match_the_header():
+    text = open(HEADER).read()
+    for name in ("RQ_MAX_HIDDEN", "RQ_QK_HEAD_DIM", "RQ_QK_MAX_HEADS"):
+        m = re.search(r"#define\s+%s\s+(\d+)" % name, text)
+        assert m and int(m.group(1)) == getattr(rq, name), name
+
+
 def test_status_strings_and_sizes(L):
     for code in range(8):
         assert L.rq_status_string(code).decode().startswith(rq.STATUS[code])
