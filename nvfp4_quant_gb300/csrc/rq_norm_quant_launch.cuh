@@ -83,7 +83,8 @@ static cudaError_t launch_staged(const NormQuantParams &p, cudaStream_t stream)
     return launch_pdl(kern, grid, kStagedThreads, smem, stream, p);
 }
 
-// Rows above 32768 elements: one CTA of kLongThreads per row, persistent grid.
+// The two-pass kernel (rows above 16384 elements with more rows than SMs, and
+// every row above 32768): one CTA of kLongThreads per row, persistent grid.
 template <typename DT, int MODE>
 static cudaError_t launch_long(const NormQuantParams &p, cudaStream_t stream)
 {

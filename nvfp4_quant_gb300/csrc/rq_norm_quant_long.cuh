@@ -1,9 +1,10 @@
 // rq_norm_quant_long.cuh -- the fused residual add + RMSNorm + quant kernel
-// for rows longer than the register-resident shapes reach (hidden above
-// 32768 elements).
+// for long rows: above 32768 elements (no register shape reaches them), and
+// above 16384 with more rows than SMs (where it measured faster than the
+// shared-memory staged kernel and the 512 x 8 register shape).
 //
-// Such a row fits neither a thread group's registers nor a CTA's shared
-// memory (4 * hidden bytes), so a CTA of kLongThreads threads owns one row at
+// Such a row fits neither a thread group's registers nor, past 16384
+// elements, a CTA's shared memory at useful occupancy, so a CTA of kLongThreads threads owns one row at
 // a time and makes two passes over global memory.  Pass 1 loads x and the
 // residual, forms residual' = dt(x + r), stores it and sums its squares.  After
 // the row reduction, pass 2 reads back the residual' vectors the thread itself
